@@ -1,0 +1,163 @@
+"""CPU oracle for the row-parallel linear layer with a reduce-scatter (float64).
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the benchmark's
+CPU-baseline leg may import this module.  It shares no code with the CUDA
+library (no kernels, headers, helpers or tables) and the library never calls
+it.  It is deliberately plain and slow: every step is written out as the
+definition states it, with library float64 matmuls as the only building block.
+
+What is computed (problem page "A fused GEMM + reduce-scatter kernel hiding 90%
+of communication on 8 H100 GPUs", sections "What is asked" and "How it gets
+verified"; FLUX page, Figure 2):
+  the tensor-parallel group has 8 ranks.  Rank r holds the K-shard A_r (columns
+  [r*K/8, (r+1)*K/8) of A) and W_r (the same rows of W) and computes the
+  partial product P_r = A_r W_r in BF16 with FP32 accumulation.  The partials
+  are summed across ranks and each rank keeps one row slice of the total: rank
+  s receives rows [s*M/8, (s+1)*M/8) (a reduce-scatter).
+
+Readings of points the pages leave open (each one is listed in the design doc):
+  * each partial is rounded to bf16 once, round to nearest even, directly from
+    its exact value (the bf16 tensor a real reduce-scatter would move);
+  * the sum over ranks is a left fold in FP32 (IEEE, round to nearest even),
+    starting from the rank-0 partial and adding ranks 1..7 in order;
+  * the FP32 total is rounded to bf16, round to nearest even;
+  * the "FP32 reference" of the correctness rule is taken in float64: the
+    unrounded sum of the exact partials.
+
+Pins that tie this module to something other than itself live in
+tests/test_oracle_pins.py (exact rational brute force, closed forms, invariants
+and library routines).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+WORLD = 8
+
+# ---------------------------------------------------------------------------
+# bf16 helpers (own implementation: 8 significant bits, exponent range of fp32)
+# ---------------------------------------------------------------------------
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round to the nearest bf16 value, ties to even, straight from the input.
+
+    The input is taken at its own precision (float64 or float32), so a float64
+    value is rounded once, not through float32.  Returns float64 values that
+    are exactly representable in bf16 (inf beyond the bf16 range, NaN kept).
+    bf16 has an 8-bit significand, so a value with binary exponent e
+    (x = m * 2**e, 0.5 <= |m| < 1) has quantum 2**(e-8); the quantum never
+    goes below the smallest subnormal, 2**-133.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    qe = np.maximum(e - 8, -133)
+    y = np.ldexp(np.rint(np.ldexp(x, -qe)), qe)  # rint rounds half to even
+    y = np.where(np.abs(y) >= 2.0 ** 128, np.copysign(np.inf, x), y)
+    return np.where(np.isfinite(x), y, x)
+
+
+def bf16_from_bits(bits) -> np.ndarray:
+    """uint16 bf16 bit patterns -> float64 values (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_to_bits(values) -> np.ndarray:
+    """bf16-representable float values -> uint16 bit patterns (exact)."""
+    v = np.asarray(values, dtype=np.float64).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# The operation
+# ---------------------------------------------------------------------------
+
+
+def rank_partials(A_shards, W_shards) -> np.ndarray:
+    """Exact per-rank partial products S_r = A_r @ W_r in float64.
+
+    A_shards: [8][M][Kr] (bf16 bits or float values), W_shards: [8][Kr][N].
+    Inputs are bf16, so every product is exact in float64 and the float64
+    matmul only rounds its running sums (relative error ~ Kr * 2**-53).
+    """
+    A = _as_values(A_shards)
+    W = _as_values(W_shards)
+    assert A.ndim == 3 and W.ndim == 3 and A.shape[0] == W.shape[0] == WORLD
+    assert A.shape[2] == W.shape[1]
+    return np.stack([A[r] @ W[r] for r in range(WORLD)])
+
+
+def reduce_partials(S: np.ndarray):
+    """Round each partial to bf16, fold in FP32 in rank order, round to bf16.
+
+    Returns (out, ref): out [M][N] float64 values on the bf16 grid, ref [M][N]
+    the unrounded float64 sum of the exact partials.
+    """
+    Q = [bf16_round(S[r]).astype(np.float32) for r in range(WORLD)]  # exact casts
+    T = Q[0].copy()
+    for r in range(1, WORLD):
+        T = (T + Q[r]).astype(np.float32)  # IEEE fp32 add, round to nearest even
+    out = bf16_round(T)
+    ref = np.zeros(S.shape[1:], dtype=np.float64)
+    for r in range(WORLD):
+        ref = ref + S[r]
+    return out, ref
+
+
+def gemm_rs(A_shards, W_shards):
+    """Full output of the row-parallel linear layer.
+
+    Returns (out, ref) as float64 arrays [M][N]; slice s of the reduce-scatter
+    is rows [s*M/8, (s+1)*M/8) of out (see slices()).
+    """
+    return reduce_partials(rank_partials(A_shards, W_shards))
+
+
+def gemm_rs_rows(A_shards, W_shards, rows):
+    """The same result evaluated only at the given output rows.
+
+    Row i of every partial depends only on row i of each A_r, so this is the
+    definition applied to a row subset (used to check sampled outputs of large
+    workloads).  Returns (out[len(rows)][N], ref[len(rows)][N]).
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    A = _as_values(A_shards)[:, rows, :]
+    return gemm_rs(A, W_shards)
+
+
+def slices(out: np.ndarray, world: int = WORLD):
+    """Split the reduced output into the per-rank row slices of the scatter."""
+    M = out.shape[0]
+    assert M % world == 0
+    h = M // world
+    return [out[s * h:(s + 1) * h] for s in range(world)]
+
+
+# ---------------------------------------------------------------------------
+# The correctness rule ("How it gets verified": BF16 tolerance, max relative
+# error at most 1.1x the unfused path against an FP32 reference)
+# ---------------------------------------------------------------------------
+
+
+def err_vs_oracle(X, out) -> float:
+    """max |X - out| / max |out| against the oracle's bf16 result."""
+    X = np.asarray(X, dtype=np.float64)
+    den = float(np.max(np.abs(out))) if out.size else 0.0
+    num = float(np.max(np.abs(X - out))) if out.size else 0.0
+    return num / den if den > 0 else num
+
+
+def rel_vs_ref(X, ref) -> float:
+    """max |X - ref| / max |ref| against the float64 (unrounded) reference."""
+    X = np.asarray(X, dtype=np.float64)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(X - ref))) if ref.size else 0.0
+    return num / den if den > 0 else num
+
+
+def _as_values(x) -> np.ndarray:
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return bf16_from_bits(x)
+    return x.astype(np.float64)
