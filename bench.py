@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the fused GEMM + reduce-scatter (row-parallel linear layer,
+8 virtual tensor-parallel ranks on one GB300).
+
+Metric (problem page "A fused GEMM + reduce-scatter kernel hiding 90% of
+communication on 8 H100 GPUs", "How it gets verified"): throughput of the
+fused kernel in TFLOP/s (2*M*N*K per step) and the overlap efficiency
+(T_gemm + T_rs - T_fused) / T_rs, medians of 200 iterations after warm-up,
+with T_gemm and T_rs the unfused path's GEMM and reduce-scatter kernels each
+timed alone.
+
+One step = one fused run over one batch of synthetic input: every rank tile of
+the GEMM, its bf16 staging write, its completion flag and the rank-order fp32
+reduction into the bf16 output.  Inputs stay resident in device memory for
+`value`; `e2e` adds, every step, the host-to-device copy of A and W from
+pinned memory and the device-to-host copy of the output, through the
+library's host-buffer entry point.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+emulated tensor-parallel group lives inside one GPU, so nothing is exchanged
+between GPUs); rank 0 prints one JSON line.  --impl reference times the CPU
+oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+reduce-scatter TFLOP/s and overlap efficiency vs unfused, 1 GB300"
+DEFAULT_WORKLOAD = "llama3_70b_o_proj_m2048"
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_SOURCES = ["tensor_gemm_reduce_gb300/csrc/kernels.cuh", "tensor_gemm_reduce_gb300/csrc/ptx.cuh",
+                  "tensor_gemm_reduce_gb300/csrc/schedule.h", "tensor_gemm_reduce_gb300/csrc/gemm_rs.cu"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--overlap-iters", type=int, default=200)
+    p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--reference-seconds", type=float, default=120.0,
+                   help="target length of the whole --impl reference run")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def source_sha256() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    sha = source_sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read()
+        m_k = re.search(r"^kernel:\s*(\S+)", text, re.M)
+        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m_s = re.search(r"^source_sha256:\s*([0-9a-f]{64})", text, re.M)
+        m_b = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_k and m_w and m_s and m_b and m_k.group(1) == kernel and m_w.group(1) == workload:
+            if m_s.group(1) == sha:
+                return float(m_b.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_QUERY}", "--format=csv",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        from tensor_gemm_reduce_gb300 import metrics
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        text = open(self.path).read()
+        os.unlink(self.path)
+        return metrics.summarize_clocks(text)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_oracle_rate(A_bits, W_bits, N, K, target_s: float, max_rows: int):
+    """Time the CPU oracle on a row sample of the workload: returns (TFLOP/s, rows, seconds)."""
+    import numpy as np
+    import oracle
+    rows = 8
+    while True:
+        idx = np.arange(rows) % max_rows
+        t0 = time.perf_counter()
+        oracle.gemm_rs_rows(A_bits, W_bits, idx)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= max_rows:
+            break
+        rows = int(min(max_rows, max(rows * 2, rows * target_s / max(dt, 1e-3) * 1.05)))
+    return 2.0 * rows * N * K / dt / 1e12, rows, dt
+
+
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on host cores."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from tensor_gemm_reduce_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    A_bits, W_bits = workloads.make_inputs(w)
+    # size each step's row sample so the whole run stays near --reference-seconds
+    t0 = time.perf_counter()
+    oracle.gemm_rs_rows(A_bits, W_bits, np.arange(8))
+    per_row = (time.perf_counter() - t0) / 8
+    total_steps = args.warmup + args.steps
+    rows = int(max(1, min(w.M, args.reference_seconds / total_steps / per_row)))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        idx = (np.arange(rows) + cursor) % w.M
+        cursor = (cursor + rows) % w.M
+        oracle.gemm_rs_rows(A_bits, W_bits, idx)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    cores = blas_threads()
+    sample = (f"{rows} of {w.M} output rows per step (all 8 ranks, full N={w.N}, K={w.K}); "
+              f"float64 numpy oracle, {cores} BLAS threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "world": 8,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from tensor_gemm_reduce_gb300 import gemm_rs as G
+    from tensor_gemm_reduce_gb300 import metrics, workloads
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    G.load_library(build_if_missing=True)
+    w = workloads.WORKLOADS[args.workload]
+    M, N, K = w.M, w.N, w.K
+    A_bits, W_bits = workloads.make_inputs(w)
+    # CPU baseline first (rank 0, one GPU): host work before the GPU gets busy
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, dt = cpu_oracle_rate(A_bits, W_bits, N, K, args.cpu_seconds, M)
+        cores = blas_threads()
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{rows} of {M} output rows of {w.name} (all 8 ranks, full N and K) in "
+                         f"{dt:.1f} s; float64 numpy oracle"}
+
+    A_host = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_host = torch.from_numpy(W_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    A = A_host.cuda()
+    W = W_host.cuda()
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    out_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    plan = G.Plan(M, N, K)
+    info = plan.info
+    ws = plan.new_workspace()
+    stream = torch.cuda.current_stream()
+
+    def check():
+        rc = plan.status()
+        if rc != G.GEMM_RS_OK:
+            raise RuntimeError(f"device status: {G.strerror(rc)}")
+
+    # sanity: fused and unfused agree bit for bit
+    plan.run(A, W, out, ws, G.FUSED)
+    check()
+    f0 = out.clone()
+    plan.run(A, W, out, ws, G.UNFUSED)
+    check()
+    if not torch.equal(f0.view(torch.int16), out.view(torch.int16)):
+        raise RuntimeError("fused and unfused outputs differ")
+
+    # overlap efficiency: per-iteration medians of each kernel alone
+    def time_mode(mode, iters, warm):
+        for _ in range(warm):
+            plan.run(A, W, out, ws, mode)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        torch.cuda.synchronize()
+        for s, e in ev:
+            s.record(stream)
+            plan.run(A, W, out, ws, mode)
+            e.record(stream)
+        torch.cuda.synchronize()
+        check()
+        return metrics.median(s.elapsed_time(e) for s, e in ev) * 1e-3
+
+    it = args.overlap_iters
+    t_gemm = time_mode(G.GEMM_ONLY, it, 20)
+    t_rs = time_mode(G.RS_ONLY, it, 20)
+    t_fused = time_mode(G.FUSED, it, 20)
+    t_unfused = time_mode(G.UNFUSED, it, 20)
+    eff = metrics.overlap_efficiency(t_gemm, t_rs, t_fused)
+
+    # the contract's timed region: K fused steps between events
+    for _ in range(args.warmup):
+        plan.run(A, W, out, ws, G.FUSED)
+    check()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            plan.run(A, W, out, ws, G.FUSED)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    check()
+    clocks = clk.summary()
+    elapsed = e0.elapsed_time(e1) * 1e-3
+
+    # end to end through the host-buffer entry point
+    h2d = A_host.numel() * 2 + W_host.numel() * 2
+    d2h = out_host.numel() * 2
+    for _ in range(3):
+        plan.run_host(A_host, W_host, out_host, A, W, out, ws, G.FUSED)
+    check()
+    ke = max(1, args.e2e_steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(ke):
+        plan.run_host(A_host, W_host, out_host, A, W, out, ws, G.FUSED)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    check()
+    e2e_elapsed = e2.elapsed_time(e3) * 1e-3
+    if not torch.equal(out_host.view(torch.int16), f0.cpu().view(torch.int16)):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
+
+    flops = metrics.gemm_flops(M, N, K)
+    elapsed, e2e_elapsed = metrics.max_over_ranks([elapsed, e2e_elapsed], device="cuda")
+    agg = metrics.aggregate_ranks([flops * args.steps] * world, [elapsed])
+    value = agg["rate"] / 1e12
+    e2e_value = flops * ke * world / e2e_elapsed / 1e12
+
+    peaks = load_peaks()
+    per_launch = elapsed / args.steps
+    long_region = elapsed > 1.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    peak_kind = ("sustained" if long_region else "burst") + f" bf16, of {peaks['source']}"
+    traffic = committed_traffic("gemm_rs_kernel_fused", w.name)
+    roof = metrics.roofline("tensor", flops / per_launch / 1e12, peak, "TFLOP/s", traffic)
+    roof["peak_kind"] = peak_kind
+    roof["kernel"] = "gemm_rs_kernel<fused>"
+    rs_gbs = metrics.rs_bytes(M, N) / t_rs / 1e9
+    rs_roof = metrics.roofline("hbm", rs_gbs, peaks["hbm_gbs"], "GB/s",
+                               committed_traffic("rs_reduce_kernel", w.name))
+    rs_roof["kernel"] = "rs_reduce_kernel (unfused path, alone)"
+    rs_roof["peak_kind"] = f"copy bandwidth, of {peaks['source']}"
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": M, "N": N, "K": K, "world": 8,
+                   "parallelism": "8 virtual TP ranks per GPU" + (f", {world} replicas" if world > 1 else ""),
+                   "l2": "no flush; inputs larger than L2 (A+W %.0f MB, staging %.0f MB written and read per step)"
+                         % ((A.numel() + W.numel()) * 2 / 1e6, info.staging_bytes / 1e6),
+                   "grid": info.grid, "threads_fused": info.threads_fused, "band_m": info.band_m,
+                   "unit_rows": info.unit_rows},
+        "overlap": {"efficiency": eff, "t_gemm_us": t_gemm * 1e6, "t_rs_us": t_rs * 1e6,
+                    "t_fused_us": t_fused * 1e6, "t_unfused_us": t_unfused * 1e6,
+                    "fused_speedup_vs_unfused": t_unfused / t_fused, "iters": it,
+                    "statistic": "median of per-iteration CUDA-event times, rank 0"},
+        "roofline": roof,
+        "rs_roofline": rs_roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": ke},
+        "gpu_launches": args.steps * info.launches[G.FUSED],
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        return run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,167 @@
+/*
+ * gemm_rs.h -- C ABI of the fused GEMM + reduce-scatter library (sm_103a).
+ *
+ * The operation (problem page "A fused GEMM + reduce-scatter kernel hiding
+ * 90% of communication on 8 H100 GPUs", sections "What is asked" and "How it
+ * gets verified"; FLUX page, abstract and Figure 2): a row-parallel linear
+ * layer under tensor parallelism of degree 8.  Rank r holds the K-shard
+ * A_r = A[:, r*K/8 : (r+1)*K/8] and W_r = W[r*K/8 : (r+1)*K/8, :], and
+ * computes the partial product P_r = A_r W_r in bf16 with fp32 accumulation.
+ * The partials are summed across the ranks (reduce) and rank s keeps rows
+ * [s*M/8, (s+1)*M/8) of the sum (scatter).
+ *
+ * On one GPU the 8 ranks are virtual.  Each rank's bf16 partial tiles are
+ * written to a separate staging region in device memory (standing in for the
+ * peer's receive buffer) and published with a per-tile completion flag.
+ * Reducers add the 8 partials of an output tile in fp32, in rank order
+ * 0..7, and round the total to bf16 (round to nearest even).
+ *
+ * Memory: the caller owns every device buffer and the CUDA stream.  The plan
+ * owns host state only.  All pointers below are device pointers unless a
+ * comment says "host".
+ *
+ * Errors: every entry point returns a gemm_rs_status code.  No C++ exception
+ * and no abort crosses this boundary.  A plan serves one stream at a time.
+ */
+#ifndef GEMM_RS_H
+#define GEMM_RS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_RS_WORLD 8
+
+/* Status codes. */
+enum gemm_rs_status {
+  GEMM_RS_OK = 0,
+  GEMM_RS_ERR_INVALID_ARG = -1,        /* null pointer, world != 8, bad mode or field */
+  GEMM_RS_ERR_UNSUPPORTED_SHAPE = -2,  /* M%8, N%8 or K%64 != 0, negative or too large */
+  GEMM_RS_ERR_UNSUPPORTED_DEVICE = -3, /* no CUDA device, or not compute capability 10.3 */
+  GEMM_RS_ERR_CUDA = -4,               /* a CUDA runtime/driver call or launch failed */
+  GEMM_RS_ERR_TIMEOUT = -5,            /* a device-side wait gave up (reported by status) */
+  GEMM_RS_ERR_MISALIGNED = -6,         /* a buffer is not 16-byte aligned */
+  GEMM_RS_ERR_WORKSPACE = -7           /* workspace pointer missing for a mode that needs it */
+};
+
+/* Execution modes of gemm_rs_run. */
+enum gemm_rs_mode {
+  GEMM_RS_FUSED = 0,     /* one persistent kernel: tile GEMM + flagged reduce-scatter */
+  GEMM_RS_UNFUSED = 1,   /* GEMM kernel writes the staging, then a separate reduce kernel */
+  GEMM_RS_GEMM_ONLY = 2, /* only the GEMM kernel (per-rank partials into staging) */
+  GEMM_RS_RS_ONLY = 3    /* only the reduce kernel (reads the staging as it is) */
+};
+
+/* Debug switches (gemm_rs_desc.debug_flags). */
+#define GEMM_RS_DEBUG_SKIP_ONE_FLAG 0x1u /* FUSED: one producer warp never publishes its
+                                            flag, so the reducers of the first output tile
+                                            time out; used to test the timeout path */
+
+/*
+ * Problem description.  Shapes: A is [8][M][K/8] bf16 (row-major, K/8
+ * contiguous: rank r's column block of A), W is [8][K/8][N] bf16 (row-major,
+ * N contiguous: rank r's row block of W), out is [M][N] bf16 row-major, whose
+ * rows [s*M/8, (s+1)*M/8) are the slice of virtual rank s.
+ */
+typedef struct gemm_rs_desc {
+  int32_t world;          /* tensor-parallel degree; must be 8 */
+  int64_t M, N, K;        /* M%8 == 0, N%8 == 0, K%64 == 0 (so K/8 is a multiple of 8); 0 allowed */
+  int32_t reducer_warps;  /* FUSED: reducer warps per CTA, 1..8; 0 = default (4) */
+  int32_t grid;           /* persistent CTAs; 0 = one per SM */
+  int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
+  int32_t unit_rows;      /* rows per reduce unit in FUSED mode: 8, 16, 32, 64 or 128; 0 = 32 */
+  uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
+  uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
+} gemm_rs_desc;
+
+typedef struct gemm_rs_plan_s* gemm_rs_t;
+
+/* Facts about a plan (for tests and benchmarks). */
+typedef struct gemm_rs_info {
+  int32_t num_sms;        /* SMs on the device */
+  int32_t grid;           /* CTAs of the GEMM / fused kernels */
+  int32_t threads_fused;  /* threads per CTA of the fused kernel */
+  int32_t threads_gemm;   /* threads per CTA of the unfused GEMM kernel */
+  int32_t smem_bytes;     /* dynamic shared memory per CTA of both GEMM kernels */
+  int32_t band_m;         /* tile-order band height in m-tiles */
+  int32_t unit_rows;      /* rows per reduce unit (FUSED) */
+  int32_t mt, nt;         /* 128-row and 256-column tiles of the output */
+  int64_t tiles;          /* 8 * mt * nt rank tiles */
+  int64_t units;          /* reduce units (FUSED) */
+  int64_t workspace_bytes;
+  int64_t staging_bytes;  /* 8 * M * N * 2 */
+  int32_t launches[4];    /* kernels launched per gemm_rs_run, indexed by mode */
+} gemm_rs_info;
+
+/*
+ * Validate d and build a plan for the current CUDA device.  On success
+ * *plan is set and *workspace_bytes (may be NULL) receives the size of the
+ * device workspace every gemm_rs_run call needs: the bf16 staging regions
+ * (8*M*N*2 bytes), the per-tile flags and a few control words.  Arguments are
+ * checked before any CUDA call, so INVALID_ARG / UNSUPPORTED_SHAPE come back
+ * on a machine without a GPU too.
+ */
+int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_bytes);
+
+/*
+ * Enqueue one execution on `stream` (a cudaStream_t; NULL = legacy default).
+ * A: [8][M][K/8] bf16, W: [8][K/8][N] bf16, out: [M][N] bf16, workspace:
+ * >= workspace_bytes, 256-byte aligned is best, 16-byte aligned is required.
+ * The caller may pass an uninitialised workspace: the first call that sees a
+ * new workspace pointer clears its control words (a small memset on the
+ * stream).  The staging part keeps the per-rank partials of the last GEMM.
+ * Returns after enqueueing; device-side failures (timeouts) are reported by
+ * gemm_rs_status.  Modes that do not read A/W (RS_ONLY) or write out
+ * (GEMM_ONLY) accept NULL for them.
+ */
+int gemm_rs_run(gemm_rs_t plan, int mode, const void* A, const void* W,
+                void* out, void* workspace, void* stream);
+
+/*
+ * Host-buffer variant of gemm_rs_run for callers whose A, W and out live in
+ * host memory.  Enqueued on `stream`, in this order: copy A_host -> A_dev
+ * (8*M*(K/8)*2 bytes) and W_host -> W_dev (8*(K/8)*N*2 bytes), run `mode`
+ * exactly as gemm_rs_run would on the device buffers, copy out_dev -> out_host
+ * (M*N*2 bytes).  All six buffers belong to the caller; host buffers should be
+ * pinned (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous,
+ * and must stay valid until the stream has passed the copies.  RS_ONLY copies
+ * nothing in, GEMM_ONLY copies nothing out.  Same return codes as gemm_rs_run,
+ * plus GEMM_RS_ERR_CUDA if a copy cannot be enqueued.
+ */
+int gemm_rs_run_host(gemm_rs_t plan, int mode, const void* A_host, const void* W_host,
+                     void* out_host, void* A_dev, void* W_dev, void* out_dev, void* workspace,
+                     void* stream);
+
+/*
+ * Synchronise `stream` and report the device error word of the workspace the
+ * plan used last: GEMM_RS_OK, GEMM_RS_ERR_TIMEOUT (a device wait gave up; the
+ * output of that run is incomplete) or GEMM_RS_ERR_CUDA.  A non-OK result
+ * also clears the workspace's control words and flags so the next run starts
+ * clean.
+ */
+int gemm_rs_status(gemm_rs_t plan, void* stream);
+
+/* Fill *info (host pointer).  */
+int gemm_rs_get_info(gemm_rs_t plan, gemm_rs_info* info);
+
+/*
+ * Tile order used by the GEMM kernels, as a host-only computation (no CUDA
+ * call): the idx-th rank tile (0 <= idx < 8*mt*nt) is rank *rank, 128-row
+ * tile *mt, 256-column tile *nt.  Uses d->band_m or the automatic band.
+ */
+int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt, int32_t* nt);
+
+/* Release the plan (host state only; device buffers stay the caller's). */
+int gemm_rs_destroy(gemm_rs_t plan);
+
+/* Static text for a status code. */
+const char* gemm_rs_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_RS_H */

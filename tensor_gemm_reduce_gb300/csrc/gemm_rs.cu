@@ -1,0 +1,408 @@
+// gemm_rs.cu -- host side of the C ABI declared in include/gemm_rs.h:
+// argument checks, workspace layout, TMA tensor maps, launch configuration,
+// the per-run epoch of the completion flags, and the device error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/gemm_rs.h"
+#include "kernels.cuh"
+
+using namespace grs;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kDefaultReducerWarps = 4;
+constexpr int kDefaultUnitRows = 32;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t staging_bytes, flags_off, flags_bytes, ctrl_off, total;
+};
+
+Layout layout_for(int64_t M, int64_t N, int64_t mt, int64_t nt) {
+  Layout l;
+  l.staging_bytes = (size_t)kWorld * (size_t)M * (size_t)N * 2;
+  l.flags_off = align_up(l.staging_bytes, 256);
+  l.flags_bytes = (size_t)kWorld * (size_t)mt * (size_t)nt * 4;
+  l.ctrl_off = align_up(l.flags_off + l.flags_bytes, 256);
+  l.total = l.ctrl_off + 256;
+  return l;
+}
+
+int check_desc(const gemm_rs_desc* d) {
+  if (!d) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->world != GEMM_RS_WORLD) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->reducer_warps < 0 || d->reducer_warps > kMaxReducerWarps) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->grid < 0 || d->band_m < 0) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->unit_rows != 0 && d->unit_rows != 8 && d->unit_rows != 16 && d->unit_rows != 32 &&
+      d->unit_rows != 64 && d->unit_rows != 128)
+    return GEMM_RS_ERR_INVALID_ARG;
+  if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  // TMA coordinates and kernel indices are 32-bit.
+  if (d->M > (1ll << 30) || d->N > (1ll << 30) || d->K / 8 > (1ll << 30))
+    return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  const int64_t mt = (d->M + kBM - 1) / kBM, nt = (d->N + kBN - 1) / kBN;
+  if (mt * nt * kWorld >= (1ll << 31)) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  return GEMM_RS_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct gemm_rs_plan_s {
+  gemm_rs_desc d;
+  int device = 0, num_sms = 0;
+  int grid = 0, reducer_warps = 0, band = 1, unit_rows = 32, units_per_region = 4;
+  int mt = 0, nt = 0, num_kb = 0;
+  long long tiles = 0, units = 0;
+  Layout lay;
+  uint32_t epoch = 0;
+  void* last_ws = nullptr;
+  const void* map_A = nullptr;
+  const void* map_W = nullptr;
+  void* map_ws = nullptr;
+  bool maps_valid = false;
+  GemmParams params;
+};
+
+extern "C" {
+
+const char* gemm_rs_strerror(int code) {
+  switch (code) {
+    case GEMM_RS_OK: return "ok";
+    case GEMM_RS_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_RS_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need M%8==0, N%8==0, K%64==0)";
+    case GEMM_RS_ERR_UNSUPPORTED_DEVICE: return "no CUDA device, or not compute capability 10.3";
+    case GEMM_RS_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case GEMM_RS_ERR_TIMEOUT: return "a device-side wait timed out; that run's output is incomplete";
+    case GEMM_RS_ERR_MISALIGNED: return "buffer not 16-byte aligned";
+    case GEMM_RS_ERR_WORKSPACE: return "workspace missing";
+    default: return "unknown status";
+  }
+}
+
+int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt,
+                     int32_t* nt) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!rank || !mt || !nt) return GEMM_RS_ERR_INVALID_ARG;
+  const int mtc = (int)((d->M + kBM - 1) / kBM), ntc = (int)((d->N + kBN - 1) / kBN);
+  const long long tiles = (long long)kWorld * mtc * ntc;
+  if (idx < 0 || idx >= tiles) return GEMM_RS_ERR_INVALID_ARG;
+  const int band = d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K);
+  const TileCoord t = tile_at(idx, mtc, ntc, band);
+  *rank = t.rank;
+  *mt = t.mt;
+  *nt = t.nt;
+  return GEMM_RS_OK;
+}
+
+int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_bytes) {
+  if (!plan) return GEMM_RS_ERR_INVALID_ARG;
+  *plan = nullptr;
+  int rc = check_desc(d);
+  if (rc) return rc;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (prop.major != 10 || prop.minor != 3) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  if (prop.sharedMemPerBlockOptin < (size_t)kSmemAlloc) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  if (cudaFuncSetAttribute(gemm_rs_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemAlloc) != cudaSuccess ||
+      cudaFuncSetAttribute(gemm_rs_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemAlloc) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
+
+  gemm_rs_plan_s* h = new (std::nothrow) gemm_rs_plan_s();
+  if (!h) return GEMM_RS_ERR_CUDA;
+  h->d = *d;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->mt = (int)((d->M + kBM - 1) / kBM);
+  h->nt = (int)((d->N + kBN - 1) / kBN);
+  h->num_kb = (int)((d->K / kWorld + kBK - 1) / kBK);
+  h->tiles = (long long)kWorld * h->mt * h->nt;
+  h->grid = d->grid > 0 ? d->grid : h->num_sms;
+  if (h->grid > h->num_sms) h->grid = h->num_sms;  // one co-resident CTA per SM
+  h->reducer_warps = d->reducer_warps > 0 ? d->reducer_warps : kDefaultReducerWarps;
+  h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt) : auto_band(d->M, d->K);
+  if (h->band < 1) h->band = 1;
+  h->unit_rows = d->unit_rows > 0 ? d->unit_rows : kDefaultUnitRows;
+  h->units_per_region = kBM / h->unit_rows;
+  h->units = (long long)h->mt * h->nt * h->units_per_region;
+  h->lay = layout_for(d->M, d->N, h->mt, h->nt);
+  if (h->d.timeout_ns == 0) h->d.timeout_ns = kDefaultTimeoutNs;
+  if (workspace_bytes) *workspace_bytes = h->lay.total;
+  *plan = h;
+  return GEMM_RS_OK;
+}
+
+int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
+  if (!h || !info) return GEMM_RS_ERR_INVALID_ARG;
+  memset(info, 0, sizeof(*info));
+  info->num_sms = h->num_sms;
+  info->grid = h->grid;
+  info->threads_fused = 32 * (kGemmWarps + h->reducer_warps);
+  info->threads_gemm = 32 * kGemmWarps;
+  info->smem_bytes = kSmemAlloc;
+  info->band_m = h->band;
+  info->unit_rows = h->unit_rows;
+  info->mt = h->mt;
+  info->nt = h->nt;
+  info->tiles = h->tiles;
+  info->units = h->units;
+  info->workspace_bytes = (int64_t)h->lay.total;
+  info->staging_bytes = (int64_t)h->lay.staging_bytes;
+  const bool empty = h->d.M == 0 || h->d.N == 0;
+  info->launches[GEMM_RS_FUSED] = empty ? 0 : 1;
+  info->launches[GEMM_RS_UNFUSED] = empty ? 0 : (h->d.K == 0 ? 1 : 2);
+  info->launches[GEMM_RS_GEMM_ONLY] = empty ? 0 : 1;
+  info->launches[GEMM_RS_RS_ONLY] = empty ? 0 : 1;
+  return GEMM_RS_OK;
+}
+
+int gemm_rs_destroy(gemm_rs_t h) {
+  delete h;
+  return GEMM_RS_OK;
+}
+
+static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)h->grid);
+  cfg.blockDim = dim3((unsigned)(32 * (kGemmWarps + (fused ? h->reducer_warps : 0))));
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  // Reducer warps wait on tiles of other CTAs: all CTAs must be co-resident.
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = fused ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = fused ? cudaLaunchKernelEx(&cfg, gemm_rs_kernel<true>, h->params)
+                        : cudaLaunchKernelEx(&cfg, gemm_rs_kernel<false>, h->params);
+  return e == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
+}
+
+static int launch_rs(gemm_rs_t h, const void* ws, void* out, cudaStream_t st) {
+  const long long mn = (long long)h->d.M * h->d.N;
+  long long nvec = mn / 8;
+  long long blocks = (nvec + 255) / 256;
+  const long long cap = (long long)h->num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  rs_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(ws),
+                                                     static_cast<uint16_t*>(out), mn);
+  return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
+}
+
+static int launch_zero(gemm_rs_t h, void* p, size_t bytes, cudaStream_t st) {
+  long long n16 = (long long)(bytes / 16);
+  long long blocks = (n16 + 255) / 256;
+  const long long cap = (long long)h->num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  zero_fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint4*>(p), n16);
+  return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
+}
+
+int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, void* ws,
+                void* stream) {
+  if (!h) return GEMM_RS_ERR_INVALID_ARG;
+  if (mode < GEMM_RS_FUSED || mode > GEMM_RS_RS_ONLY) return GEMM_RS_ERR_INVALID_ARG;
+  const gemm_rs_desc& d = h->d;
+  if (d.M == 0 || d.N == 0) return GEMM_RS_OK;  // nothing to read or write
+  // A and W hold no element when K == 0: their pointers are not used then.
+  const bool needs_ab = mode != GEMM_RS_RS_ONLY && d.K > 0;
+  const bool needs_out = mode != GEMM_RS_GEMM_ONLY;
+  if (!ws) return GEMM_RS_ERR_WORKSPACE;
+  if ((needs_ab && (!A || !W)) || (needs_out && !out)) return GEMM_RS_ERR_INVALID_ARG;
+  if (!aligned16(ws) || (needs_ab && (!aligned16(A) || !aligned16(W))) ||
+      (needs_out && !aligned16(out)))
+    return GEMM_RS_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return GEMM_RS_ERR_INVALID_ARG;
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  if (ws != h->last_ws) {
+    // first use of this workspace: clear flags and control words
+    if (cudaMemsetAsync(wsb + h->lay.flags_off, 0, h->lay.total - h->lay.flags_off, st) !=
+        cudaSuccess)
+      return GEMM_RS_ERR_CUDA;
+    h->last_ws = ws;
+    h->epoch = 0;
+  }
+
+  if (d.K == 0) {  // empty contraction: every partial and the sum are zero
+    if (mode == GEMM_RS_GEMM_ONLY) return launch_zero(h, wsb, h->lay.staging_bytes, st);
+    if (mode == GEMM_RS_RS_ONLY) return launch_rs(h, wsb, out, st);
+    return launch_zero(h, out, (size_t)d.M * d.N * 2, st);
+  }
+
+  if (!h->maps_valid || (needs_ab && (A != h->map_A || W != h->map_W)) || ws != h->map_ws) {
+    GemmParams& p = h->params;
+    memset(&p, 0, sizeof(p));
+    const uint64_t Kr = (uint64_t)(d.K / kWorld);
+    const void* a = needs_ab ? A : h->map_A;
+    const void* w = needs_ab ? W : h->map_W;
+    if (a && w) {
+      if (!make_map(&p.tmap_a, a, Kr, (uint64_t)d.M, kWorld, Kr * 2, Kr * 2 * (uint64_t)d.M, kBK,
+                    kBM) ||
+          !make_map(&p.tmap_b, w, (uint64_t)d.N, Kr, kWorld, (uint64_t)d.N * 2,
+                    (uint64_t)d.N * 2 * Kr, 64, kBK))
+        return GEMM_RS_ERR_CUDA;
+    }
+    if (!make_map(&p.tmap_st, wsb, (uint64_t)d.N, (uint64_t)d.M, kWorld, (uint64_t)d.N * 2,
+                  (uint64_t)d.N * 2 * (uint64_t)d.M, 64, 32))
+      return GEMM_RS_ERR_CUDA;
+    p.stage = reinterpret_cast<const uint16_t*>(wsb);
+    p.flags = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
+    p.ctrl = reinterpret_cast<uint32_t*>(wsb + h->lay.ctrl_off);
+    p.M = (int)d.M;
+    p.N = (int)d.N;
+    p.Kr = (int)Kr;
+    p.mt_count = h->mt;
+    p.nt_count = h->nt;
+    p.band = h->band;
+    p.num_kb = h->num_kb;
+    p.unit_rows = h->unit_rows;
+    p.units_per_region = h->units_per_region;
+    p.num_tiles = h->tiles;
+    p.num_units = h->units;
+    p.debug_flags = d.debug_flags;
+    p.timeout_ns = d.timeout_ns;
+    h->map_A = a;
+    h->map_W = w;
+    h->map_ws = ws;
+    h->maps_valid = a && w;
+  }
+  h->params.out = static_cast<uint16_t*>(out);
+
+  int rc = GEMM_RS_OK;
+  switch (mode) {
+    case GEMM_RS_FUSED:
+      h->epoch += 1;
+      h->params.flag_target = (uint32_t)kEpiWarps * h->epoch;
+      rc = launch_gemm(h, true, st);
+      break;
+    case GEMM_RS_UNFUSED:
+      rc = launch_gemm(h, false, st);
+      if (rc == GEMM_RS_OK) rc = launch_rs(h, wsb, out, st);
+      break;
+    case GEMM_RS_GEMM_ONLY:
+      rc = launch_gemm(h, false, st);
+      break;
+    case GEMM_RS_RS_ONLY:
+      rc = launch_rs(h, wsb, out, st);
+      break;
+  }
+  if (rc != GEMM_RS_OK) cudaGetLastError();
+  return rc;
+}
+
+int gemm_rs_status(gemm_rs_t h, void* stream) {
+  if (!h) return GEMM_RS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
+  if (!h->last_ws) return GEMM_RS_OK;
+  uint32_t words[kCtrlWords];
+  uint8_t* wsb = static_cast<uint8_t*>(h->last_ws);
+  if (cudaMemcpyAsync(words, wsb + h->lay.ctrl_off, sizeof(words), cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
+  if (words[kCtrlError] == 0) return GEMM_RS_OK;
+  // Start clean: zero flags and control words, restart the epoch.
+  if (cudaMemsetAsync(wsb + h->lay.flags_off, 0, h->lay.total - h->lay.flags_off, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
+  h->epoch = 0;
+  return GEMM_RS_ERR_TIMEOUT;
+}
+
+}  // extern "C"
+
+extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const void* W_host,
+                                void* out_host, void* A_dev, void* W_dev, void* out_dev,
+                                void* ws, void* stream) {
+  if (!h) return GEMM_RS_ERR_INVALID_ARG;
+  if (mode < GEMM_RS_FUSED || mode > GEMM_RS_RS_ONLY) return GEMM_RS_ERR_INVALID_ARG;
+  const bool needs_ab = mode != GEMM_RS_RS_ONLY;
+  const bool needs_out = mode != GEMM_RS_GEMM_ONLY;
+  const gemm_rs_desc& d = h->d;
+  const size_t a_bytes = (size_t)d.M * (size_t)d.K * 2;  // 8 shards of M x K/8
+  const size_t w_bytes = (size_t)d.K * (size_t)d.N * 2;  // 8 shards of K/8 x N
+  const size_t o_bytes = (size_t)d.M * (size_t)d.N * 2;
+  if ((needs_ab && a_bytes && (!A_host || !A_dev)) || (needs_ab && w_bytes && (!W_host || !W_dev)) ||
+      (needs_out && o_bytes && (!out_host || !out_dev)))
+    return GEMM_RS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (needs_ab && a_bytes &&
+      cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return cudaGetLastError(), GEMM_RS_ERR_CUDA;
+  if (needs_ab && w_bytes &&
+      cudaMemcpyAsync(W_dev, W_host, w_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return cudaGetLastError(), GEMM_RS_ERR_CUDA;
+  int rc = gemm_rs_run(h, mode, A_dev, W_dev, out_dev, ws, stream);
+  if (rc != GEMM_RS_OK) return rc;
+  if (needs_out && o_bytes &&
+      cudaMemcpyAsync(out_host, out_dev, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return cudaGetLastError(), GEMM_RS_ERR_CUDA;
+  return GEMM_RS_OK;
+}

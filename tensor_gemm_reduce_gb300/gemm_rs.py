@@ -1,0 +1,306 @@
+"""Python binding of the C ABI in include/gemm_rs.h (ctypes; marshalling only).
+
+Every step of the operation runs in the CUDA library; this module checks
+tensor shapes, dtypes and devices, passes raw pointers and the current CUDA
+stream, and turns status codes into exceptions.  If the library is missing
+the import of the binding fails loudly: there is no fallback path.
+
+Layouts (problem page "A fused GEMM + reduce-scatter kernel hiding 90% of
+communication on 8 H100 GPUs", "What is asked"; FLUX page, Figure 2):
+  A   [8][M][K/8] bf16  rank r's column block of the activations
+  W   [8][K/8][N] bf16  rank r's row block of the weight
+  out [M][N]      bf16  rows [s*M/8, (s+1)*M/8) are virtual rank s's slice
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+from . import build as _build
+
+WORLD = 8
+
+GEMM_RS_OK = 0
+GEMM_RS_ERR_INVALID_ARG = -1
+GEMM_RS_ERR_UNSUPPORTED_SHAPE = -2
+GEMM_RS_ERR_UNSUPPORTED_DEVICE = -3
+GEMM_RS_ERR_CUDA = -4
+GEMM_RS_ERR_TIMEOUT = -5
+GEMM_RS_ERR_MISALIGNED = -6
+GEMM_RS_ERR_WORKSPACE = -7
+
+FUSED, UNFUSED, GEMM_ONLY, RS_ONLY = 0, 1, 2, 3
+MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": RS_ONLY}
+
+DEBUG_SKIP_ONE_FLAG = 0x1
+
+
+class gemm_rs_desc(ctypes.Structure):
+    _fields_ = [
+        ("world", ctypes.c_int32),
+        ("M", ctypes.c_int64),
+        ("N", ctypes.c_int64),
+        ("K", ctypes.c_int64),
+        ("reducer_warps", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("band_m", ctypes.c_int32),
+        ("unit_rows", ctypes.c_int32),
+        ("timeout_ns", ctypes.c_uint64),
+        ("debug_flags", ctypes.c_uint32),
+    ]
+
+
+class gemm_rs_info(ctypes.Structure):
+    _fields_ = [
+        ("num_sms", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("threads_fused", ctypes.c_int32),
+        ("threads_gemm", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32),
+        ("band_m", ctypes.c_int32),
+        ("unit_rows", ctypes.c_int32),
+        ("mt", ctypes.c_int32),
+        ("nt", ctypes.c_int32),
+        ("tiles", ctypes.c_int64),
+        ("units", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64),
+        ("staging_bytes", ctypes.c_int64),
+        ("launches", ctypes.c_int32 * 4),
+    ]
+
+    def as_dict(self):
+        d = {f: getattr(self, f) for f, _ in self._fields_ if f != "launches"}
+        d["launches"] = list(self.launches)
+        return d
+
+
+class GemmRSError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+# Every entry point declared in include/gemm_rs.h with its ctypes signature.
+_SIGS = {
+    "gemm_rs_create": (ctypes.c_int, [ctypes.POINTER(gemm_rs_desc), ctypes.POINTER(ctypes.c_void_p),
+                                      ctypes.POINTER(ctypes.c_size_t)]),
+    "gemm_rs_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "gemm_rs_run_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 8),
+    "gemm_rs_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "gemm_rs_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(gemm_rs_info)]),
+    "gemm_rs_schedule": (ctypes.c_int, [ctypes.POINTER(gemm_rs_desc), ctypes.c_int64,
+                                        ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                        ctypes.POINTER(ctypes.c_int32)]),
+    "gemm_rs_destroy": (ctypes.c_int, [ctypes.c_void_p]),
+    "gemm_rs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgemm_rs.so (building it first if asked and needed)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = _build.LIB
+    if build_if_missing and (not os.path.exists(path)):
+        _build.build_library()
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built: {path} (run tensor_gemm_reduce_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def header_symbols(header_path: Optional[str] = None):
+    """Names of the functions declared in include/gemm_rs.h."""
+    if header_path is None:
+        header_path = os.path.join(_build.ROOT, "include", "gemm_rs.h")
+    text = open(header_path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_rs_[a-z_]+)\s*\(", text)))
+
+
+def strerror(code: int) -> str:
+    try:
+        return load_library(build_if_missing=False).gemm_rs_strerror(code).decode()
+    except Exception:
+        return f"status {code}"
+
+
+def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
+          world=WORLD):
+    return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns, debug_flags)
+
+
+# ----------------------------------------------------------------------------
+# thin wrappers with the C names
+# ----------------------------------------------------------------------------
+
+
+def gemm_rs_create(desc: gemm_rs_desc):
+    """Returns (plan handle, workspace bytes); raises GemmRSError."""
+    lib = load_library()
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    rc = lib.gemm_rs_create(ctypes.byref(desc), ctypes.byref(h), ctypes.byref(ws))
+    if rc != GEMM_RS_OK:
+        raise GemmRSError(rc, "gemm_rs_create")
+    return h, ws.value
+
+
+def gemm_rs_run(plan, mode: int, A_ptr: int, W_ptr: int, out_ptr: int, ws_ptr: int, stream_ptr: int) -> int:
+    return load_library().gemm_rs_run(plan, mode, A_ptr, W_ptr, out_ptr, ws_ptr, stream_ptr)
+
+
+def gemm_rs_run_host(plan, mode: int, A_host: int, W_host: int, out_host: int, A_dev: int, W_dev: int,
+                     out_dev: int, ws_ptr: int, stream_ptr: int) -> int:
+    return load_library().gemm_rs_run_host(plan, mode, A_host, W_host, out_host, A_dev, W_dev,
+                                           out_dev, ws_ptr, stream_ptr)
+
+
+def gemm_rs_status(plan, stream_ptr: int) -> int:
+    return load_library().gemm_rs_status(plan, stream_ptr)
+
+
+def gemm_rs_get_info(plan) -> gemm_rs_info:
+    info = gemm_rs_info()
+    rc = load_library().gemm_rs_get_info(plan, ctypes.byref(info))
+    if rc != GEMM_RS_OK:
+        raise GemmRSError(rc, "gemm_rs_get_info")
+    return info
+
+
+def gemm_rs_schedule(desc: gemm_rs_desc, idx: int):
+    r, m, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    rc = load_library().gemm_rs_schedule(ctypes.byref(desc), idx, ctypes.byref(r), ctypes.byref(m),
+                                         ctypes.byref(n))
+    if rc != GEMM_RS_OK:
+        raise GemmRSError(rc, "gemm_rs_schedule")
+    return r.value, m.value, n.value
+
+
+def gemm_rs_destroy(plan) -> int:
+    return load_library().gemm_rs_destroy(plan)
+
+
+def gemm_rs_strerror(code: int) -> str:
+    return strerror(code)
+
+
+# ----------------------------------------------------------------------------
+# torch-facing plan object
+# ----------------------------------------------------------------------------
+
+
+class Plan:
+    """A plan for one (M, N, K) on the current CUDA device."""
+
+    def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
+                 band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0):
+        self.M, self.N, self.K = int(M), int(N), int(K)
+        self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
+                          timeout_ns, debug_flags)
+        self._h, self.workspace_bytes = gemm_rs_create(self.desc)
+
+    @property
+    def info(self) -> gemm_rs_info:
+        return gemm_rs_get_info(self._h)
+
+    def new_workspace(self, device=None):
+        import torch
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        return torch.empty(self.workspace_bytes, dtype=torch.uint8, device=dev)
+
+    def _check(self, t, shape, name):
+        import torch
+        if t is None:
+            return 0
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        return t.data_ptr()
+
+    def run(self, A, W, out, workspace, mode: int = FUSED, stream=None) -> None:
+        import torch
+        Kr = self.K // WORLD
+        a = self._check(A, (WORLD, self.M, Kr), "A")
+        w = self._check(W, (WORLD, Kr, self.N), "W")
+        o = self._check(out, (self.M, self.N), "out")
+        if workspace is None or workspace.numel() * workspace.element_size() < self.workspace_bytes:
+            raise ValueError("workspace missing or too small")
+        s = stream if stream is not None else torch.cuda.current_stream()
+        rc = gemm_rs_run(self._h, int(mode), a, w, o, workspace.data_ptr(), s.cuda_stream)
+        if rc != GEMM_RS_OK:
+            raise GemmRSError(rc, "gemm_rs_run")
+
+    def run_host(self, A_host, W_host, out_host, A, W, out, workspace, mode: int = FUSED,
+                 stream=None) -> None:
+        """Host tensors in (pinned for asynchronous copies), host tensor out; the
+        copies and the run are enqueued on one stream by the library."""
+        import torch
+        Kr = self.K // WORLD
+        for t, shape, name in ((A_host, (WORLD, self.M, Kr), "A_host"),
+                               (W_host, (WORLD, Kr, self.N), "W_host"),
+                               (out_host, (self.M, self.N), "out_host")):
+            if t.dtype != torch.bfloat16 or tuple(t.shape) != shape or t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host bf16 tensor of shape {shape}")
+        a = self._check(A, (WORLD, self.M, Kr), "A")
+        w = self._check(W, (WORLD, Kr, self.N), "W")
+        o = self._check(out, (self.M, self.N), "out")
+        if workspace is None or workspace.numel() * workspace.element_size() < self.workspace_bytes:
+            raise ValueError("workspace missing or too small")
+        s = stream if stream is not None else torch.cuda.current_stream()
+        rc = gemm_rs_run_host(self._h, int(mode), A_host.data_ptr(), W_host.data_ptr(),
+                              out_host.data_ptr(), a, w, o, workspace.data_ptr(), s.cuda_stream)
+        if rc != GEMM_RS_OK:
+            raise GemmRSError(rc, "gemm_rs_run_host")
+
+    def status(self, stream=None) -> int:
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return gemm_rs_status(self._h, s.cuda_stream)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            gemm_rs_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Plan] = None):
+    """One call of the row-parallel linear layer with reduce-scatter.
+
+    Returns (out, plan, workspace); out[s*M/8:(s+1)*M/8] is rank s's slice.
+    """
+    import torch
+    R, M, Kr = A.shape
+    N = W.shape[2]
+    if plan is None:
+        plan = Plan(M, N, Kr * R)
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    if workspace is None:
+        workspace = plan.new_workspace(A.device)
+    plan.run(A, W, out, workspace, mode)
+    return out, plan, workspace

@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and
+exports every function include/gemm_rs.h declares, arguments are rejected
+before any CUDA call, and the tile order covers every rank tile once with the
+8 rank tiles of a region next to each other."""
+import ctypes
+
+import pytest
+
+from tensor_gemm_reduce_gb300 import gemm_rs as G
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tensor_gemm_reduce_gb300 import build
+    build.build_library()
+    return G.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = G.header_symbols()
+    assert set(names) >= {"gemm_rs_create", "gemm_rs_run", "gemm_rs_destroy", "gemm_rs_status",
+                          "gemm_rs_strerror", "gemm_rs_get_info", "gemm_rs_schedule"}
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(G._SIGS), "binding signatures and header out of sync"
+
+
+def _create(**kw):
+    d = G._desc(kw.pop("M", 128), kw.pop("N", 256), kw.pop("K", 512), **kw)
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    return G.load_library().gemm_rs_create(ctypes.byref(d), ctypes.byref(h), ctypes.byref(ws))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(world=4), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(reducer_warps=9), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(reducer_warps=-1), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(unit_rows=12), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(grid=-2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
+    (dict(N=12), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
+    (dict(K=96), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
+    (dict(M=-8), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
+    (dict(M=1 << 31), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
+])
+def test_create_rejects_bad_arguments(lib, kw, code):
+    assert _create(**kw) == code
+
+
+def test_null_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.gemm_rs_create(None, ctypes.byref(h), None) == G.GEMM_RS_ERR_INVALID_ARG
+    d = G._desc(128, 256, 512)
+    assert lib.gemm_rs_create(ctypes.byref(d), None, None) == G.GEMM_RS_ERR_INVALID_ARG
+    assert lib.gemm_rs_run(None, 0, None, None, None, None, None) == G.GEMM_RS_ERR_INVALID_ARG
+    assert lib.gemm_rs_status(None, None) == G.GEMM_RS_ERR_INVALID_ARG
+    assert lib.gemm_rs_get_info(None, None) == G.GEMM_RS_ERR_INVALID_ARG
+    assert lib.gemm_rs_destroy(None) == G.GEMM_RS_OK
+
+
+def test_strerror(lib):
+    for code in range(-7, 1):
+        assert G.strerror(code) and G.strerror(code) != f"status {code}"
+    assert G.strerror(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("M,N,K,band", [(128, 512, 1024, 0), (392, 776, 1600, 0),
+                                        (2048, 8192, 8192, 0), (8192, 8192, 28672, 0),
+                                        (1000, 6144, 6144, 3), (520, 1000, 1024, 1)])
+def test_schedule_covers_every_tile_once(lib, M, N, K, band):
+    d = G._desc(M, N, K, band_m=band)
+    mt, nt = (M + 127) // 128, (N + 255) // 256
+    seen = set()
+    order = []
+    for i in range(8 * mt * nt):
+        r, m, n = G.gemm_rs_schedule(d, i)
+        assert 0 <= r < 8 and 0 <= m < mt and 0 <= n < nt
+        seen.add((r, m, n))
+        order.append((r, m, n))
+    assert len(seen) == 8 * mt * nt
+    # the 8 rank tiles of a region are consecutive, ranks in order
+    for g in range(mt * nt):
+        blk = order[8 * g: 8 * g + 8]
+        assert [b[0] for b in blk] == list(range(8))
+        assert len({(b[1], b[2]) for b in blk}) == 1
+    with pytest.raises(G.GemmRSError):
+        G.gemm_rs_schedule(d, 8 * mt * nt)
+
+
+def test_schedule_band_walks_columns_inside_band(lib):
+    # band of 4 tile rows: positions 0..3 are column 0, rows 0..3
+    d = G._desc(1024, 1024, 1024, band_m=4)
+    regions = [G.gemm_rs_schedule(d, 8 * g)[1:] for g in range(8 * 4)]
+    assert regions[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
+    assert regions[16] == (4, 0)
+
+
+def test_auto_band_keeps_a_rows_within_budget(lib):
+    for M, K in [(2048, 8192), (8192, 28672), (32768, 16384), (512, 6144)]:
+        d = G._desc(M, 1024, K)
+        # find the band: the first region that is in column 1
+        mt = (M + 127) // 128
+        band = None
+        for g in range(mt * 4):
+            _, m, n = G.gemm_rs_schedule(d, 8 * g)
+            if n == 1:
+                band = g
+                break
+        band = band if band is not None else mt
+        assert 1 <= band <= mt
+        assert band == mt or band * 128 * K * 2 <= 32 << 20
