@@ -62,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--reference-seconds", type=float, default=120.0,
                    help="target length of the whole --impl reference run")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", choices=["fused", "unfused", "gemm_only", "rs_only"], default=None,
+                   help="only run --warmup + --steps launches of one mode (a target for ncu)")
     return p.parse_args(argv)
 
 
@@ -395,11 +397,39 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def run_profile_target(args, local):
+    """Warm-up plus timed launches of one mode and nothing else, for ncu."""
+    import numpy as np
+    import torch
+    from tensor_gemm_reduce_gb300 import gemm_rs as G
+    from tensor_gemm_reduce_gb300 import workloads
+    torch.cuda.set_device(local)
+    w = workloads.WORKLOADS[args.workload]
+    A_bits, W_bits = workloads.make_inputs(w)
+    A = torch.from_numpy(A_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    W = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+    plan = G.Plan(w.M, w.N, w.K)
+    ws = plan.new_workspace()
+    mode = G.MODES[args.profile]
+    if mode == G.RS_ONLY:
+        plan.run(A, W, out, ws, G.GEMM_ONLY)
+    for _ in range(args.warmup + args.steps):
+        plan.run(A, W, out, ws, mode)
+    rc = plan.status()
+    if rc != G.GEMM_RS_OK:
+        raise RuntimeError(G.strerror(rc))
+    print(json.dumps({"profile": args.profile, "workload": w.name, "launches": args.warmup + args.steps}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.profile:
+        return run_profile_target(args, local)
     if world > 1:
         import torch
         import torch.distributed as dist
