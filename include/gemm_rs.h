@@ -44,7 +44,8 @@ enum gemm_rs_status {
   GEMM_RS_ERR_CUDA = -4,               /* a CUDA runtime/driver call or launch failed */
   GEMM_RS_ERR_TIMEOUT = -5,            /* a device-side wait gave up (reported by status) */
   GEMM_RS_ERR_MISALIGNED = -6,         /* a buffer is not 16-byte aligned */
-  GEMM_RS_ERR_WORKSPACE = -7           /* workspace pointer missing for a mode that needs it */
+  GEMM_RS_ERR_WORKSPACE = -7,          /* workspace pointer missing for a mode that needs it */
+  GEMM_RS_ERR_TOO_LARGE = -8           /* beyond the fixed scratch of gemm_rs_fused_noalloc */
 };
 
 /* Execution modes of gemm_rs_run. */
@@ -153,6 +154,40 @@ int gemm_rs_get_info(gemm_rs_t plan, gemm_rs_info* info);
  * tile *mt, 256-column tile *nt.  Uses d->band_m or the automatic band.
  */
 int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt, int32_t* nt);
+
+/*
+ * Fused run that allocates nothing.  The pages have no counterpart: this is a
+ * convenience of this library for callers that cannot allocate device memory
+ * when they call it -- a plug-in that runs inside a host application which
+ * owns the whole device-memory budget, or a latency-bound serving path that
+ * allows no cudaMalloc once it is up (a cudaMalloc may synchronise the device
+ * and cost milliseconds).  Such a caller passes only its inputs and its
+ * output; the staging regions, flags and control words live in one static
+ * device array of this library (32 MiB of staging plus 64 KiB of flags and
+ * 256 bytes of control words), which every GPU that loads the library keeps
+ * until the process exits.
+ *
+ * Same operation, layouts and kernel as gemm_rs_run(..., GEMM_RS_FUSED, ...)
+ * with the default plan settings.  Limits: 8*M*N*2 bytes of staging must fit
+ * in 32 MiB (M*N <= 2,097,152) and 8*ceil(M/128)*ceil(N/256) flags in 64 KiB;
+ * larger problems return GEMM_RS_ERR_TOO_LARGE before touching the GPU.
+ * Shape rules and the other return codes are those of gemm_rs_create and
+ * gemm_rs_run.
+ *
+ * error_word: optional device pointer to 4 bytes; after the run the stream
+ * copies the device error bits of this call there (0 = ok, non-zero = a
+ * device-side wait timed out and the output is incomplete).
+ *
+ * The first call on a device sets up that device (looks up the array's
+ * device address, sets the kernel's shared-memory limit); make that first
+ * call before any stream capture.  Every call clears the flags and control
+ * words it uses on the stream, then reuses the array, which keeps the last
+ * call's contents.  Calls share that one array: calls that can overlap on
+ * the GPU (different streams, or several host threads) race and produce
+ * garbage; order them on one stream.
+ */
+int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, int64_t M, int64_t N,
+                          int64_t K, void* error_word, void* stream);
 
 /* Release the plan (host state only; device buffers stay the caller's). */
 int gemm_rs_destroy(gemm_rs_t plan);

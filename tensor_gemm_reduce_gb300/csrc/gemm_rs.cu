@@ -7,6 +7,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/gemm_rs.h"
@@ -114,6 +115,8 @@ const char* gemm_rs_strerror(int code) {
     case GEMM_RS_ERR_TIMEOUT: return "a device-side wait timed out; that run's output is incomplete";
     case GEMM_RS_ERR_MISALIGNED: return "buffer not 16-byte aligned";
     case GEMM_RS_ERR_WORKSPACE: return "workspace missing";
+    case GEMM_RS_ERR_TOO_LARGE:
+      return "problem larger than the static scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
@@ -404,5 +407,159 @@ extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const
   if (needs_out && o_bytes &&
       cudaMemcpyAsync(out_host, out_dev, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return cudaGetLastError(), GEMM_RS_ERR_CUDA;
+  return GEMM_RS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// No-allocation entry point (gemm_rs_fused_noalloc).
+//
+// For callers that may not allocate device memory when they call in (a
+// plug-in inside an application that owns the device-memory budget, a serving
+// path that forbids cudaMalloc after start-up).  The fused kernel's scratch --
+// bf16 staging, per-tile flags, control words -- lives in the file-scope array
+// below instead of a caller workspace.  Host code never uses the array's name
+// as an address (in host code it is only a stand-in for the device symbol):
+// the first call on a device looks up the real device address with
+// cudaGetSymbolAddress while that device is current and keeps it.
+namespace {
+constexpr size_t kNoallocStagingBytes = (size_t)32 << 20;  // 8*M*N*2 <= 32 MiB
+constexpr size_t kNoallocFlagBytes = (size_t)64 << 10;     // 8*regions*4 <= 64 KiB
+constexpr size_t kNoallocCtrlBytes = 256;
+constexpr size_t kNoallocBytes = kNoallocStagingBytes + kNoallocFlagBytes + kNoallocCtrlBytes;
+constexpr int kNoallocMaxDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocBytes];
+
+namespace {
+struct NoallocDevice {
+  bool ready;
+  uint8_t* scratch;  // device address of g_noalloc_scratch on this device
+  int num_sms;
+};
+NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current.
+int noalloc_setup(int dev, const NoallocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (major != 10 || minor != 3) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return GEMM_RS_ERR_CUDA;
+    }
+    if (cudaFuncSetAttribute(gemm_rs_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_RS_ERR_CUDA;
+    }
+    d.scratch = static_cast<uint8_t*>(p);
+    d.num_sms = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return GEMM_RS_OK;
+}
+}  // namespace
+
+extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, int64_t M, int64_t N,
+                                     int64_t K, void* error_word, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || M % 8 || N % 8 || K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  if (M > (1ll << 30) || N > (1ll << 30)) return GEMM_RS_ERR_TOO_LARGE;
+  const int64_t mt = (M + kBM - 1) / kBM, nt = (N + kBN - 1) / kBN;
+  const size_t staging = (size_t)kWorld * (size_t)M * (size_t)N * 2;
+  const size_t flag_bytes = (size_t)kWorld * (size_t)mt * (size_t)nt * 4;
+  if (staging > kNoallocStagingBytes || flag_bytes > kNoallocFlagBytes) return GEMM_RS_ERR_TOO_LARGE;
+  const bool empty = M == 0 || N == 0;
+  if (!empty && (!out || (K > 0 && (!A || !W)))) return GEMM_RS_ERR_INVALID_ARG;
+  if ((!empty && !aligned16(out)) || (!empty && K > 0 && (!aligned16(A) || !aligned16(W))) ||
+      (error_word && (reinterpret_cast<uintptr_t>(error_word) & 3u)))
+    return GEMM_RS_ERR_MISALIGNED;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  }
+  const NoallocDevice* nd = nullptr;
+  int rc = noalloc_setup(dev, &nd);
+  if (rc != GEMM_RS_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* scratch = nd->scratch;
+  uint32_t* flags = reinterpret_cast<uint32_t*>(scratch + kNoallocStagingBytes);
+  uint32_t* ctrl = reinterpret_cast<uint32_t*>(scratch + kNoallocStagingBytes + kNoallocFlagBytes);
+
+  // The array keeps the previous call's contents: the flags of this problem
+  // and the control words must start at zero.
+  if ((flag_bytes && cudaMemsetAsync(flags, 0, flag_bytes, st) != cudaSuccess) ||
+      cudaMemsetAsync(ctrl, 0, kNoallocCtrlBytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
+
+  if (!empty && K == 0) {  // empty contraction: the sum is zero
+    const long long n16 = M * N * 2 / 16;
+    long long blocks = (n16 + 255) / 256;
+    if (blocks > (long long)nd->num_sms * 8) blocks = (long long)nd->num_sms * 8;
+    zero_fill_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<uint4*>(out), n16);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_RS_ERR_CUDA;
+  } else if (!empty) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const uint64_t Kr = (uint64_t)(K / kWorld);
+    if (!make_map(&p.tmap_a, A, Kr, (uint64_t)M, kWorld, Kr * 2, Kr * 2 * (uint64_t)M, kBK, kBM) ||
+        !make_map(&p.tmap_b, W, (uint64_t)N, Kr, kWorld, (uint64_t)N * 2, (uint64_t)N * 2 * Kr, 64,
+                  kBK) ||
+        !make_map(&p.tmap_st, scratch, (uint64_t)N, (uint64_t)M, kWorld, (uint64_t)N * 2,
+                  (uint64_t)N * 2 * (uint64_t)M, 64, 32))
+      return GEMM_RS_ERR_CUDA;
+    p.stage = reinterpret_cast<const uint16_t*>(scratch);
+    p.out = static_cast<uint16_t*>(out);
+    p.flags = flags;
+    p.ctrl = ctrl;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.Kr = (int)Kr;
+    p.mt_count = (int)mt;
+    p.nt_count = (int)nt;
+    p.band = auto_band(M, K);
+    p.num_kb = (int)((Kr + kBK - 1) / kBK);
+    p.unit_rows = kDefaultUnitRows;
+    p.units_per_region = kBM / kDefaultUnitRows;
+    p.num_tiles = (long long)kWorld * mt * nt;
+    p.num_units = (long long)mt * nt * p.units_per_region;
+    p.flag_target = (uint32_t)kEpiWarps;  // flags were just cleared: one run's worth
+    p.timeout_ns = kDefaultTimeoutNs;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)nd->num_sms);
+    cfg.blockDim = dim3((unsigned)(32 * (kGemmWarps + kDefaultReducerWarps)));
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_rs_kernel<true>, p) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_RS_ERR_CUDA;
+    }
+  }
+  if (error_word && cudaMemcpyAsync(error_word, ctrl + kCtrlError, sizeof(uint32_t),
+                                    cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
   return GEMM_RS_OK;
 }

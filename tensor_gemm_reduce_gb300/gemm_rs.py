@@ -30,6 +30,10 @@ GEMM_RS_ERR_CUDA = -4
 GEMM_RS_ERR_TIMEOUT = -5
 GEMM_RS_ERR_MISALIGNED = -6
 GEMM_RS_ERR_WORKSPACE = -7
+GEMM_RS_ERR_TOO_LARGE = -8
+
+# Fixed scratch of the no-allocation entry point (see gemm_rs_fused_noalloc).
+NOALLOC_STAGING_BYTES = 32 << 20
 
 FUSED, UNFUSED, GEMM_ONLY, RS_ONLY = 0, 1, 2, 3
 MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": RS_ONLY}
@@ -96,6 +100,9 @@ _SIGS = {
     "gemm_rs_schedule": (ctypes.c_int, [ctypes.POINTER(gemm_rs_desc), ctypes.c_int64,
                                         ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                         ctypes.POINTER(ctypes.c_int32)]),
+    "gemm_rs_fused_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_void_p, ctypes.c_void_p]),
     "gemm_rs_destroy": (ctypes.c_int, [ctypes.c_void_p]),
     "gemm_rs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -190,6 +197,16 @@ def gemm_rs_schedule(desc: gemm_rs_desc, idx: int):
     if rc != GEMM_RS_OK:
         raise GemmRSError(rc, "gemm_rs_schedule")
     return r.value, m.value, n.value
+
+
+def gemm_rs_fused_noalloc(A_ptr: int, W_ptr: int, out_ptr: int, M: int, N: int, K: int,
+                          error_word_ptr: int, stream_ptr: int) -> int:
+    """Fused run with the library's static scratch instead of a workspace: for
+    callers that may not allocate device memory at call time.  Returns the
+    status code; the device error bits of the call land in *error_word_ptr
+    (a 4-byte device buffer, or 0 for none)."""
+    return load_library().gemm_rs_fused_noalloc(A_ptr, W_ptr, out_ptr, M, N, K, error_word_ptr,
+                                                stream_ptr)
 
 
 def gemm_rs_destroy(plan) -> int:
