@@ -60,6 +60,10 @@ enum gemm_rs_mode {
 #define GEMM_RS_DEBUG_SKIP_ONE_FLAG 0x1u /* FUSED: one producer warp never publishes its
                                             flag, so the reducers of the first output tile
                                             time out; used to test the timeout path */
+#define GEMM_RS_DEBUG_NO_STAGING_L2 0x2u /* FUSED: store staging tiles without the L2
+                                            evict-last hint and keep them after reduction
+                                            (by default reduced staging lines are dropped
+                                            from L2 unwritten; needs N % 64 == 0) */
 
 /*
  * Problem description.  Shapes: A is [8][M][K/8] bf16 (row-major, K/8
@@ -73,9 +77,11 @@ typedef struct gemm_rs_desc {
   int32_t reducer_warps;  /* FUSED: reducer warps per CTA, 1..8; 0 = default (4) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
-  int32_t unit_rows;      /* rows per reduce unit in FUSED mode: 8, 16, 32, 64 or 128; 0 = 32 */
+  int32_t unit_rows;      /* rows per reduce unit in FUSED mode: 8, 16, 32, 64 or 128; 0 = 16 */
   uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
   uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
+  int32_t mma_ctas;       /* CTAs per MMA tile: 1 (128 x 256 tiles) or 2 (a 2-CTA cluster
+                             computes 256 x 256 tiles); 0 = 2 */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -89,12 +95,14 @@ typedef struct gemm_rs_info {
   int32_t smem_bytes;     /* dynamic shared memory per CTA of both GEMM kernels */
   int32_t band_m;         /* tile-order band height in m-tiles */
   int32_t unit_rows;      /* rows per reduce unit (FUSED) */
-  int32_t mt, nt;         /* 128-row and 256-column tiles of the output */
+  int32_t mt, nt;         /* tile rows (of tile_rows rows) and 256-column tiles of the output */
   int64_t tiles;          /* 8 * mt * nt rank tiles */
   int64_t units;          /* reduce units (FUSED) */
   int64_t workspace_bytes;
   int64_t staging_bytes;  /* 8 * M * N * 2 */
   int32_t launches[4];    /* kernels launched per gemm_rs_run, indexed by mode */
+  int32_t mma_ctas;       /* CTAs per MMA tile */
+  int32_t tile_rows;      /* output rows of one rank tile: 128 * mma_ctas */
 } gemm_rs_info;
 
 /*
@@ -113,7 +121,9 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
  * >= workspace_bytes, 256-byte aligned is best, 16-byte aligned is required.
  * The caller may pass an uninitialised workspace: the first call that sees a
  * new workspace pointer clears its control words (a small memset on the
- * stream).  The staging part keeps the per-rank partials of the last GEMM.
+ * stream).  After GEMM_ONLY or UNFUSED the staging part holds the per-rank
+ * partials of that GEMM; after FUSED it holds no defined values (reduced
+ * staging lines are dropped from L2 without write-back when N % 64 == 0).
  * Returns after enqueueing; device-side failures (timeouts) are reported by
  * gemm_rs_status.  Modes that do not read A/W (RS_ONLY) or write out
  * (GEMM_ONLY) accept NULL for them.
@@ -150,8 +160,9 @@ int gemm_rs_get_info(gemm_rs_t plan, gemm_rs_info* info);
 
 /*
  * Tile order used by the GEMM kernels, as a host-only computation (no CUDA
- * call): the idx-th rank tile (0 <= idx < 8*mt*nt) is rank *rank, 128-row
- * tile *mt, 256-column tile *nt.  Uses d->band_m or the automatic band.
+ * call): the idx-th rank tile (0 <= idx < 8*mt*nt) is rank *rank, tile row
+ * *mt (rows [mt*T, (mt+1)*T) with T = 128 * mma_ctas), 256-column tile *nt.
+ * Uses d->band_m or the automatic band.
  */
 int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt, int32_t* nt);
 

@@ -19,7 +19,8 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultReducerWarps = 4;
-constexpr int kDefaultUnitRows = 32;
+constexpr int kDefaultUnitRows = 16;
+constexpr int kDefaultMmaCtas = 2;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -45,6 +46,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->unit_rows != 0 && d->unit_rows != 8 && d->unit_rows != 16 && d->unit_rows != 32 &&
       d->unit_rows != 64 && d->unit_rows != 128)
     return GEMM_RS_ERR_INVALID_ARG;
+  if (d->mma_ctas < 0 || d->mma_ctas > 2) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   // TMA coordinates and kernel indices are 32-bit.
@@ -85,12 +87,93 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int mma_ctas_of(const gemm_rs_desc* d) { return d->mma_ctas > 0 ? d->mma_ctas : kDefaultMmaCtas; }
+
+const void* gemm_kernel(bool fused, int pair) {
+  if (pair == 2)
+    return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 2>)
+                 : reinterpret_cast<const void*>(gemm_rs_kernel<false, 2>);
+  return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 1>)
+               : reinterpret_cast<const void*>(gemm_rs_kernel<false, 1>);
+}
+
+int gemm_smem(int pair) { return pair == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc; }
+
+void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, bool fused,
+                 int grid, int threads, cudaStream_t st) {
+  memset(cfg, 0, sizeof(*cfg));
+  cfg->gridDim = dim3((unsigned)grid);
+  cfg->blockDim = dim3((unsigned)threads);
+  cfg->dynamicSmemBytes = (size_t)gemm_smem(pair);
+  cfg->stream = st;
+  int n = 0;
+  // Reducer warps wait on tiles of other CTAs: all CTAs must be co-resident.
+  attr[n].id = cudaLaunchAttributeCooperative;
+  attr[n].val.cooperative = fused ? 1 : 0;
+  ++n;
+  if (pair == 2) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg->attrs = attr;
+  cfg->numAttrs = n;
+}
+
+// One launch of the persistent GEMM kernel (fused or GEMM only).
+int launch_gemm_kernel(int pair, bool fused, int grid, int threads, const GemmParams& p,
+                       cudaStream_t st) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  fill_launch(&cfg, attr, pair, fused, grid, threads, st);
+  void* args[] = {const_cast<GemmParams*>(&p)};
+  if (cudaLaunchKernelExC(&cfg, gemm_kernel(fused, pair), args) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_RS_ERR_CUDA;
+  }
+  return GEMM_RS_OK;
+}
+
+// Set the shared-memory limit of the four GEMM kernels; persistent grid size
+// (CTAs) for `pair` CTAs per MMA: one CTA per SM, whole clusters only.
+int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_fused, int* grid) {
+  for (int pr = 1; pr <= 2; ++pr)
+    for (int f = 0; f < 2; ++f)
+      if (cudaFuncSetAttribute(gemm_kernel(f != 0, pr), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               gemm_smem(pr)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_RS_ERR_CUDA;
+      }
+  (void)dev;
+  int g = requested > 0 && requested < num_sms ? requested : num_sms;
+  if (pair == 2) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_launch(&cfg, attr, 2, false, 2 * (num_sms / 2), threads_fused, 0);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel(true, 2), &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_RS_ERR_CUDA;
+    }
+    if (clusters < 1) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+    int pairs = g / 2;
+    if (pairs > clusters) pairs = clusters;
+    if (pairs < 1) pairs = 1;
+    g = 2 * pairs;
+  }
+  *grid = g;
+  return GEMM_RS_OK;
+}
+
 }  // namespace
 
 struct gemm_rs_plan_s {
   gemm_rs_desc d;
   int device = 0, num_sms = 0;
-  int grid = 0, reducer_warps = 0, band = 1, unit_rows = 32, units_per_region = 4;
+  int pair = 2, tile_rows = 256;
+  int grid = 0, reducer_warps = 0, band = 1, unit_rows = 16, units_per_region = 16;
   int mt = 0, nt = 0, num_kb = 0;
   long long tiles = 0, units = 0;
   Layout lay;
@@ -126,10 +209,12 @@ int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t*
   int rc = check_desc(d);
   if (rc) return rc;
   if (!rank || !mt || !nt) return GEMM_RS_ERR_INVALID_ARG;
-  const int mtc = (int)((d->M + kBM - 1) / kBM), ntc = (int)((d->N + kBN - 1) / kBN);
+  const int tile_rows = kBM * mma_ctas_of(d);
+  const int mtc = (int)((d->M + tile_rows - 1) / tile_rows), ntc = (int)((d->N + kBN - 1) / kBN);
   const long long tiles = (long long)kWorld * mtc * ntc;
   if (idx < 0 || idx >= tiles) return GEMM_RS_ERR_INVALID_ARG;
-  const int band = d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K);
+  const int band =
+      d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K, tile_rows);
   const TileCoord t = tile_at(idx, mtc, ntc, band);
   *rank = t.rank;
   *mt = t.mt;
@@ -154,31 +239,32 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
     return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
   }
   if (prop.major != 10 || prop.minor != 3) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
-  if (prop.sharedMemPerBlockOptin < (size_t)kSmemAlloc) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
-  if (cudaFuncSetAttribute(gemm_rs_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemAlloc) != cudaSuccess ||
-      cudaFuncSetAttribute(gemm_rs_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemAlloc) != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_RS_ERR_CUDA;
-  }
+  const int pair = mma_ctas_of(d);
+  if (prop.sharedMemPerBlockOptin < (size_t)gemm_smem(pair)) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  const int reducer_warps = d->reducer_warps > 0 ? d->reducer_warps : kDefaultReducerWarps;
+  int grid = 0;
+  rc = prepare_kernels(dev, prop.multiProcessorCount, pair, d->grid,
+                       32 * (kGemmWarps + reducer_warps), &grid);
+  if (rc) return rc;
 
   gemm_rs_plan_s* h = new (std::nothrow) gemm_rs_plan_s();
   if (!h) return GEMM_RS_ERR_CUDA;
   h->d = *d;
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
-  h->mt = (int)((d->M + kBM - 1) / kBM);
+  h->pair = pair;
+  h->tile_rows = kBM * pair;
+  h->mt = (int)((d->M + h->tile_rows - 1) / h->tile_rows);
   h->nt = (int)((d->N + kBN - 1) / kBN);
   h->num_kb = (int)((d->K / kWorld + kBK - 1) / kBK);
   h->tiles = (long long)kWorld * h->mt * h->nt;
-  h->grid = d->grid > 0 ? d->grid : h->num_sms;
-  if (h->grid > h->num_sms) h->grid = h->num_sms;  // one co-resident CTA per SM
-  h->reducer_warps = d->reducer_warps > 0 ? d->reducer_warps : kDefaultReducerWarps;
-  h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt) : auto_band(d->M, d->K);
+  h->grid = grid;
+  h->reducer_warps = reducer_warps;
+  h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt)
+                          : auto_band(d->M, d->K, h->tile_rows);
   if (h->band < 1) h->band = 1;
   h->unit_rows = d->unit_rows > 0 ? d->unit_rows : kDefaultUnitRows;
-  h->units_per_region = kBM / h->unit_rows;
+  h->units_per_region = h->tile_rows / h->unit_rows;
   h->units = (long long)h->mt * h->nt * h->units_per_region;
   h->lay = layout_for(d->M, d->N, h->mt, h->nt);
   if (h->d.timeout_ns == 0) h->d.timeout_ns = kDefaultTimeoutNs;
@@ -194,7 +280,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->grid = h->grid;
   info->threads_fused = 32 * (kGemmWarps + h->reducer_warps);
   info->threads_gemm = 32 * kGemmWarps;
-  info->smem_bytes = kSmemAlloc;
+  info->smem_bytes = gemm_smem(h->pair);
   info->band_m = h->band;
   info->unit_rows = h->unit_rows;
   info->mt = h->mt;
@@ -208,6 +294,8 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->launches[GEMM_RS_UNFUSED] = empty ? 0 : (h->d.K == 0 ? 1 : 2);
   info->launches[GEMM_RS_GEMM_ONLY] = empty ? 0 : 1;
   info->launches[GEMM_RS_RS_ONLY] = empty ? 0 : 1;
+  info->mma_ctas = h->pair;
+  info->tile_rows = h->tile_rows;
   return GEMM_RS_OK;
 }
 
@@ -217,21 +305,8 @@ int gemm_rs_destroy(gemm_rs_t h) {
 }
 
 static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)h->grid);
-  cfg.blockDim = dim3((unsigned)(32 * (kGemmWarps + (fused ? h->reducer_warps : 0))));
-  cfg.dynamicSmemBytes = kSmemAlloc;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  // Reducer warps wait on tiles of other CTAs: all CTAs must be co-resident.
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = fused ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = fused ? cudaLaunchKernelEx(&cfg, gemm_rs_kernel<true>, h->params)
-                        : cudaLaunchKernelEx(&cfg, gemm_rs_kernel<false>, h->params);
-  return e == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
+  return launch_gemm_kernel(h->pair, fused, h->grid,
+                            32 * (kGemmWarps + (fused ? h->reducer_warps : 0)), h->params, st);
 }
 
 static int launch_rs(gemm_rs_t h, const void* ws, void* out, cudaStream_t st) {
@@ -318,6 +393,7 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     p.num_kb = h->num_kb;
     p.unit_rows = h->unit_rows;
     p.units_per_region = h->units_per_region;
+    p.tile_rows = h->tile_rows;
     p.num_tiles = h->tiles;
     p.num_units = h->units;
     p.debug_flags = d.debug_flags;
@@ -332,15 +408,18 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
   int rc = GEMM_RS_OK;
   switch (mode) {
     case GEMM_RS_FUSED:
+      h->params.staging_in_l2 = (d.N % 64 == 0) && !(d.debug_flags & GEMM_RS_DEBUG_NO_STAGING_L2);
       h->epoch += 1;
-      h->params.flag_target = (uint32_t)kEpiWarps * h->epoch;
+      h->params.flag_target = (uint32_t)(kEpiWarps * h->pair) * h->epoch;
       rc = launch_gemm(h, true, st);
       break;
     case GEMM_RS_UNFUSED:
+      h->params.staging_in_l2 = 0;
       rc = launch_gemm(h, false, st);
       if (rc == GEMM_RS_OK) rc = launch_rs(h, wsb, out, st);
       break;
     case GEMM_RS_GEMM_ONLY:
+      h->params.staging_in_l2 = 0;
       rc = launch_gemm(h, false, st);
       break;
     case GEMM_RS_RS_ONLY:
@@ -436,6 +515,7 @@ struct NoallocDevice {
   bool ready;
   uint8_t* scratch;  // device address of g_noalloc_scratch on this device
   int num_sms;
+  int grid;
 };
 NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
 std::mutex g_noalloc_mu;
@@ -458,13 +538,13 @@ int noalloc_setup(int dev, const NoallocDevice** out) {
       cudaGetLastError();
       return GEMM_RS_ERR_CUDA;
     }
-    if (cudaFuncSetAttribute(gemm_rs_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_RS_ERR_CUDA;
-    }
+    int grid = 0;
+    const int rc = prepare_kernels(dev, sms, kDefaultMmaCtas, 0,
+                                   32 * (kGemmWarps + kDefaultReducerWarps), &grid);
+    if (rc != GEMM_RS_OK) return rc;
     d.scratch = static_cast<uint8_t*>(p);
     d.num_sms = sms;
+    d.grid = grid;
     d.ready = true;
   }
   *out = &d;
@@ -476,7 +556,8 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
                                      int64_t K, void* error_word, void* stream) {
   if (M < 0 || N < 0 || K < 0 || M % 8 || N % 8 || K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (M > (1ll << 30) || N > (1ll << 30)) return GEMM_RS_ERR_TOO_LARGE;
-  const int64_t mt = (M + kBM - 1) / kBM, nt = (N + kBN - 1) / kBN;
+  const int tile_rows = kBM * kDefaultMmaCtas;
+  const int64_t mt = (M + tile_rows - 1) / tile_rows, nt = (N + kBN - 1) / kBN;
   const size_t staging = (size_t)kWorld * (size_t)M * (size_t)N * 2;
   const size_t flag_bytes = (size_t)kWorld * (size_t)mt * (size_t)nt * 4;
   if (staging > kNoallocStagingBytes || flag_bytes > kNoallocFlagBytes) return GEMM_RS_ERR_TOO_LARGE;
@@ -532,29 +613,19 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.Kr = (int)Kr;
     p.mt_count = (int)mt;
     p.nt_count = (int)nt;
-    p.band = auto_band(M, K);
+    p.band = auto_band(M, K, tile_rows);
     p.num_kb = (int)((Kr + kBK - 1) / kBK);
     p.unit_rows = kDefaultUnitRows;
-    p.units_per_region = kBM / kDefaultUnitRows;
+    p.units_per_region = tile_rows / kDefaultUnitRows;
+    p.tile_rows = tile_rows;
     p.num_tiles = (long long)kWorld * mt * nt;
     p.num_units = (long long)mt * nt * p.units_per_region;
-    p.flag_target = (uint32_t)kEpiWarps;  // flags were just cleared: one run's worth
+    // flags were just cleared: one run's worth of adds
+    p.flag_target = (uint32_t)(kEpiWarps * kDefaultMmaCtas);
     p.timeout_ns = kDefaultTimeoutNs;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)nd->num_sms);
-    cfg.blockDim = dim3((unsigned)(32 * (kGemmWarps + kDefaultReducerWarps)));
-    cfg.dynamicSmemBytes = kSmemAlloc;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_rs_kernel<true>, p) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_RS_ERR_CUDA;
-    }
+    rc = launch_gemm_kernel(kDefaultMmaCtas, true, nd->grid,
+                            32 * (kGemmWarps + kDefaultReducerWarps), p, st);
+    if (rc != GEMM_RS_OK) return rc;
   }
   if (error_word && cudaMemcpyAsync(error_word, ctrl + kCtrlError, sizeof(uint32_t),
                                     cudaMemcpyDeviceToDevice, st) != cudaSuccess) {

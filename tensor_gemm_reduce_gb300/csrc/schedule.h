@@ -64,11 +64,12 @@ GRS_HD TileCoord tile_at(int64_t idx, int mt_count, int nt_count, int band) {
   return t;
 }
 
-// Automatic band height: keep the band's rows of A (all ranks, full K) at or
-// under ~32 MiB of the 126 MiB L2, and no taller than the output.
-GRS_HD int auto_band(int64_t M, int64_t K) {
-  const int64_t mt_count = (M + kBM - 1) / kBM;
-  const int64_t per_tile_row = (int64_t)kBM * K * 2;  // bytes of A per 128-row band row
+// Automatic band height, in tile rows of tile_rows output rows: keep the
+// band's rows of A (all ranks, full K) at or under ~32 MiB of the 126 MiB L2,
+// and no taller than the output.
+GRS_HD int auto_band(int64_t M, int64_t K, int tile_rows = kBM) {
+  const int64_t mt_count = (M + tile_rows - 1) / tile_rows;
+  const int64_t per_tile_row = (int64_t)tile_rows * K * 2;  // bytes of A per band row
   int64_t b = per_tile_row > 0 ? ((int64_t)32 << 20) / per_tile_row : mt_count;
   if (b < 1) b = 1;
   if (b > mt_count) b = mt_count;

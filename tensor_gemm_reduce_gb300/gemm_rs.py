@@ -39,6 +39,7 @@ FUSED, UNFUSED, GEMM_ONLY, RS_ONLY = 0, 1, 2, 3
 MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": RS_ONLY}
 
 DEBUG_SKIP_ONE_FLAG = 0x1
+DEBUG_NO_STAGING_L2 = 0x2
 
 
 class gemm_rs_desc(ctypes.Structure):
@@ -53,6 +54,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("unit_rows", ctypes.c_int32),
         ("timeout_ns", ctypes.c_uint64),
         ("debug_flags", ctypes.c_uint32),
+        ("mma_ctas", ctypes.c_int32),
     ]
 
 
@@ -72,6 +74,8 @@ class gemm_rs_info(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("staging_bytes", ctypes.c_int64),
         ("launches", ctypes.c_int32 * 4),
+        ("mma_ctas", ctypes.c_int32),
+        ("tile_rows", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -148,8 +152,9 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          world=WORLD):
-    return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns, debug_flags)
+          mma_ctas=0, world=WORLD):
+    return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
+                        debug_flags, mma_ctas)
 
 
 # ----------------------------------------------------------------------------
@@ -226,10 +231,11 @@ class Plan:
     """A plan for one (M, N, K) on the current CUDA device."""
 
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
-                 band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0):
+                 band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
+                 mma_ctas: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
-                          timeout_ns, debug_flags)
+                          timeout_ns, debug_flags, mma_ctas)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property

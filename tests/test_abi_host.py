@@ -38,6 +38,7 @@ def _create(**kw):
     (dict(reducer_warps=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(unit_rows=12), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(grid=-2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(mma_ctas=3), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(N=12), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(K=96), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
@@ -65,12 +66,14 @@ def test_strerror(lib):
     assert G.strerror(-99) == "unknown status"
 
 
+@pytest.mark.parametrize("ctas", [1, 2])
 @pytest.mark.parametrize("M,N,K,band", [(128, 512, 1024, 0), (392, 776, 1600, 0),
                                         (2048, 8192, 8192, 0), (8192, 8192, 28672, 0),
                                         (1000, 6144, 6144, 3), (520, 1000, 1024, 1)])
-def test_schedule_covers_every_tile_once(lib, M, N, K, band):
-    d = G._desc(M, N, K, band_m=band)
-    mt, nt = (M + 127) // 128, (N + 255) // 256
+def test_schedule_covers_every_tile_once(lib, M, N, K, band, ctas):
+    d = G._desc(M, N, K, band_m=band, mma_ctas=ctas)
+    rows = 128 * ctas
+    mt, nt = (M + rows - 1) // rows, (N + 255) // 256
     seen = set()
     order = []
     for i in range(8 * mt * nt):
@@ -90,17 +93,19 @@ def test_schedule_covers_every_tile_once(lib, M, N, K, band):
 
 def test_schedule_band_walks_columns_inside_band(lib):
     # band of 4 tile rows: positions 0..3 are column 0, rows 0..3
-    d = G._desc(1024, 1024, 1024, band_m=4)
+    d = G._desc(1024, 1024, 1024, band_m=4, mma_ctas=1)
     regions = [G.gemm_rs_schedule(d, 8 * g)[1:] for g in range(8 * 4)]
     assert regions[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
     assert regions[16] == (4, 0)
 
 
-def test_auto_band_keeps_a_rows_within_budget(lib):
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_auto_band_keeps_a_rows_within_budget(lib, ctas):
+    rows = 128 * ctas
     for M, K in [(2048, 8192), (8192, 28672), (32768, 16384), (512, 6144)]:
-        d = G._desc(M, 1024, K)
+        d = G._desc(M, 1024, K, mma_ctas=ctas)
         # find the band: the first region that is in column 1
-        mt = (M + 127) // 128
+        mt = (M + rows - 1) // rows
         band = None
         for g in range(mt * 4):
             _, m, n = G.gemm_rs_schedule(d, 8 * g)
@@ -109,4 +114,4 @@ def test_auto_band_keeps_a_rows_within_budget(lib):
                 break
         band = band if band is not None else mt
         assert 1 <= band <= mt
-        assert band == mt or band * 128 * K * 2 <= 32 << 20
+        assert band == mt or band * rows * K * 2 <= 32 << 20

@@ -29,7 +29,8 @@ def _full_check(A_bits, W_bits, check_partials=True, **kw):
     out, ref = oracle.reduce_partials(S)
     fv = to_host_values(fused)
     assert_parity(fv, out, ref)
-    if check_partials:
+    if check_partials:  # the staging holds defined partials after GEMM_ONLY (not after FUSED)
+        c.run(G.GEMM_ONLY, poison=True)
         partial_ulp_check(to_host_values(c.staging()), S, abs_partials(A_bits, W_bits), c.Kr)
     unf = c.run(G.UNFUSED, poison=True)
     assert torch.equal(fused.view(torch.int16), unf.view(torch.int16)), "fused != unfused bitwise"
@@ -39,9 +40,10 @@ def _full_check(A_bits, W_bits, check_partials=True, **kw):
     return c, fv, out
 
 
-def test_tiny_workload():
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_tiny_workload(ctas):
     A, W = workloads.make_inputs(workloads.TINY)
-    _full_check(A, W)
+    _full_check(A, W, mma_ctas=ctas)
 
 
 @pytest.mark.parametrize("M,N,K", [
@@ -54,13 +56,19 @@ def test_tiny_workload():
 def test_ragged_and_small_shapes(M, N, K):
     A, W = workloads.make_shape_inputs(M, N, K, seed=M + N + K)
     _full_check(A, W)
+    _full_check(A, W, mma_ctas=1)
 
 
 @pytest.mark.parametrize("kw", [dict(reducer_warps=1), dict(reducer_warps=8), dict(grid=3),
                                 dict(band_m=1), dict(unit_rows=8), dict(unit_rows=128),
-                                dict(grid=1, reducer_warps=2)])
+                                dict(grid=1, reducer_warps=2),
+                                dict(debug_flags=G.DEBUG_NO_STAGING_L2),
+                                dict(mma_ctas=1), dict(mma_ctas=1, unit_rows=32, grid=5),
+                                dict(mma_ctas=2, band_m=1, unit_rows=64)])
 def test_plan_variants(kw):
     A, W = workloads.make_shape_inputs(520, 1000, 1024, seed=9)
+    _full_check(A, W, **kw)
+    A, W = workloads.make_shape_inputs(264, 1536, 2048, seed=10)  # N % 64 == 0: staging kept in L2
     _full_check(A, W, **kw)
 
 
@@ -102,6 +110,7 @@ def test_single_nonzero_rank():
                 A2[r] = 0
         c = Case(A2, W_sh)
         got = to_host_values(c.run(G.FUSED, poison=True))
+        c.run(G.GEMM_ONLY)
         stage = to_host_values(c.staging())
         assert np.array_equal(got, stage[q])  # the sum of one partial and seven zeros
         S = oracle.rank_partials(A2, W_sh)
@@ -196,3 +205,4 @@ def test_argument_errors_on_device():
     assert p.status() == G.GEMM_RS_OK
     info = p.info
     assert info.grid >= 1 and info.smem_bytes <= 232448 and info.launches[G.UNFUSED] == 2
+    assert info.mma_ctas == 2 and info.tile_rows == 256 and info.grid % 2 == 0
