@@ -45,7 +45,9 @@ enum gemm_rs_status {
   GEMM_RS_ERR_TIMEOUT = -5,            /* a device-side wait gave up (reported by status) */
   GEMM_RS_ERR_MISALIGNED = -6,         /* a buffer is not 16-byte aligned */
   GEMM_RS_ERR_WORKSPACE = -7,          /* workspace pointer missing for a mode that needs it */
-  GEMM_RS_ERR_TOO_LARGE = -8           /* beyond the fixed scratch of gemm_rs_fused_noalloc */
+  GEMM_RS_ERR_TOO_LARGE = -8,          /* beyond the fixed scratch of gemm_rs_fused_noalloc */
+  GEMM_RS_ERR_INCOMPLETE = -9          /* a fused run ended with output blocks never reduced
+                                          (some rank tile's completion never arrived) */
 };
 
 /* Execution modes of gemm_rs_run. */
@@ -58,12 +60,19 @@ enum gemm_rs_mode {
 
 /* Debug switches (gemm_rs_desc.debug_flags). */
 #define GEMM_RS_DEBUG_SKIP_ONE_FLAG 0x1u /* FUSED: one producer warp never publishes its
-                                            flag, so the reducers of the first output tile
-                                            time out; used to test the timeout path */
+                                            completion, so its block is never queued, the
+                                            reducer waiting for it gives up after
+                                            timeout_ns and the run reports
+                                            GEMM_RS_ERR_TIMEOUT; tests the bounded wait */
 #define GEMM_RS_DEBUG_NO_STAGING_L2 0x2u /* FUSED: store staging tiles without the L2
                                             evict-last hint and keep them after reduction
                                             (by default reduced staging lines are dropped
                                             from L2 unwritten; needs N % 64 == 0) */
+#define GEMM_RS_DEBUG_TRACE 0x4u         /* GEMM kernels write, per CTA, four global-timer
+                                            stamps (ns, u64): start, epilogue done with its
+                                            tiles, MMA issue drained, all warps done; at
+                                            workspace + gemm_rs_info.trace_offset (up to
+                                            1024 CTAs) */
 
 /*
  * Problem description.  Shapes: A is [8][M][K/8] bf16 (row-major, K/8
@@ -74,10 +83,10 @@ enum gemm_rs_mode {
 typedef struct gemm_rs_desc {
   int32_t world;          /* tensor-parallel degree; must be 8 */
   int64_t M, N, K;        /* M%8 == 0, N%8 == 0, K%64 == 0 (so K/8 is a multiple of 8); 0 allowed */
-  int32_t reducer_warps;  /* FUSED: reducer warps per CTA, 1..8; 0 = default (4) */
+  int32_t reducer_warps;  /* FUSED: reducer warps per CTA, 1..6; 0 = default (4) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
-  int32_t unit_rows;      /* rows per reduce unit in FUSED mode: 8, 16, 32, 64 or 128; 0 = 16 */
+  int32_t unit_rows;      /* rows per reduce item in FUSED mode: 8, 16 or 32; 0 = 16 */
   uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
   uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
   int32_t mma_ctas;       /* CTAs per MMA tile: 1 (128 x 256 tiles) or 2 (a 2-CTA cluster
@@ -97,19 +106,21 @@ typedef struct gemm_rs_info {
   int32_t unit_rows;      /* rows per reduce unit (FUSED) */
   int32_t mt, nt;         /* tile rows (of tile_rows rows) and 256-column tiles of the output */
   int64_t tiles;          /* 8 * mt * nt rank tiles */
-  int64_t units;          /* reduce units (FUSED) */
+  int64_t units;          /* reduce items per FUSED run */
   int64_t workspace_bytes;
   int64_t staging_bytes;  /* 8 * M * N * 2 */
   int32_t launches[4];    /* kernels launched per gemm_rs_run, indexed by mode */
   int32_t mma_ctas;       /* CTAs per MMA tile */
   int32_t tile_rows;      /* output rows of one rank tile: 128 * mma_ctas */
+  int64_t trace_offset;   /* byte offset of the GEMM_RS_DEBUG_TRACE stamps in the workspace */
 } gemm_rs_info;
 
 /*
  * Validate d and build a plan for the current CUDA device.  On success
  * *plan is set and *workspace_bytes (may be NULL) receives the size of the
  * device workspace every gemm_rs_run call needs: the bf16 staging regions
- * (8*M*N*2 bytes), the per-tile flags and a few control words.  Arguments are
+ * (8*M*N*2 bytes), the per-block completion counts, the reduce-item FIFO and
+ * a few control words.  Arguments are
  * checked before any CUDA call, so INVALID_ARG / UNSUPPORTED_SHAPE come back
  * on a machine without a GPU too.
  */
@@ -149,7 +160,8 @@ int gemm_rs_run_host(gemm_rs_t plan, int mode, const void* A_host, const void* W
 /*
  * Synchronise `stream` and report the device error word of the workspace the
  * plan used last: GEMM_RS_OK, GEMM_RS_ERR_TIMEOUT (a device wait gave up; the
- * output of that run is incomplete) or GEMM_RS_ERR_CUDA.  A non-OK result
+ * output of that run is incomplete), GEMM_RS_ERR_INCOMPLETE (the run ended
+ * with output blocks that never received all 8 partials) or GEMM_RS_ERR_CUDA.  A non-OK result
  * also clears the workspace's control words and flags so the next run starts
  * clean.
  */
@@ -174,13 +186,14 @@ int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t*
  * allows no cudaMalloc once it is up (a cudaMalloc may synchronise the device
  * and cost milliseconds).  Such a caller passes only its inputs and its
  * output; the staging regions, flags and control words live in one static
- * device array of this library (32 MiB of staging plus 64 KiB of flags and
- * 256 bytes of control words), which every GPU that loads the library keeps
- * until the process exits.
+ * device array of this library (32 MiB of staging plus 4 MiB of completion
+ * counts and reduce-item slots and 2 KiB of control words), which every GPU
+ * that loads the library keeps until the process exits.
  *
  * Same operation, layouts and kernel as gemm_rs_run(..., GEMM_RS_FUSED, ...)
  * with the default plan settings.  Limits: 8*M*N*2 bytes of staging must fit
- * in 32 MiB (M*N <= 2,097,152) and 8*ceil(M/128)*ceil(N/256) flags in 64 KiB;
+ * in 32 MiB (M*N <= 2,097,152), and the 128-byte completion count plus up
+ * to 256 bytes of reduce-item slots per 32 x 256 output block in 4 MiB;
  * larger problems return GEMM_RS_ERR_TOO_LARGE before touching the GPU.
  * Shape rules and the other return codes are those of gemm_rs_create and
  * gemm_rs_run.

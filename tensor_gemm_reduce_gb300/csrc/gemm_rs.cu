@@ -25,16 +25,20 @@ constexpr int kDefaultMmaCtas = 2;
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t staging_bytes, flags_off, flags_bytes, ctrl_off, total;
+  size_t staging_bytes, flags_off, flags_bytes, queue_off, ctrl_off, trace_off, total;
 };
 
-Layout layout_for(int64_t M, int64_t N, int64_t mt, int64_t nt) {
+// blocks: 32-row blocks of the output (completion counts); items: reduce items
+// of a run (FIFO slots)
+Layout layout_for(int64_t M, int64_t N, int64_t blocks, int64_t items) {
   Layout l;
   l.staging_bytes = (size_t)kWorld * (size_t)M * (size_t)N * 2;
   l.flags_off = align_up(l.staging_bytes, 256);
-  l.flags_bytes = (size_t)kWorld * (size_t)mt * (size_t)nt * 4;
-  l.ctrl_off = align_up(l.flags_off + l.flags_bytes, 256);
-  l.total = l.ctrl_off + 256;
+  l.flags_bytes = (size_t)blocks * kFlagStride * 4;
+  l.queue_off = align_up(l.flags_off + l.flags_bytes, 256);
+  l.ctrl_off = align_up(l.queue_off + (size_t)items * kQueueStride * 8, 256);
+  l.trace_off = l.ctrl_off + (size_t)kCtrlWords * 4;
+  l.total = l.trace_off + (size_t)kMaxTraceCtas * kTraceWords * 8;
   return l;
 }
 
@@ -43,8 +47,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->world != GEMM_RS_WORLD) return GEMM_RS_ERR_INVALID_ARG;
   if (d->reducer_warps < 0 || d->reducer_warps > kMaxReducerWarps) return GEMM_RS_ERR_INVALID_ARG;
   if (d->grid < 0 || d->band_m < 0) return GEMM_RS_ERR_INVALID_ARG;
-  if (d->unit_rows != 0 && d->unit_rows != 8 && d->unit_rows != 16 && d->unit_rows != 32 &&
-      d->unit_rows != 64 && d->unit_rows != 128)
+  if (d->unit_rows != 0 && d->unit_rows != 8 && d->unit_rows != 16 && d->unit_rows != 32)
     return GEMM_RS_ERR_INVALID_ARG;
   if (d->mma_ctas < 0 || d->mma_ctas > 2) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
@@ -89,6 +92,22 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int mma_ctas_of(const gemm_rs_desc* d) { return d->mma_ctas > 0 ? d->mma_ctas : kDefaultMmaCtas; }
 
+// First region completed by the last wave of tiles (tiles are claimed in
+// order, `lanes` at a time; a region's 8 rank tiles are consecutive).
+long long tail_region_of(long long tiles, long long lanes, long long regions) {
+  long long first_last_wave_tile = tiles - lanes;
+  if (first_last_wave_tile < 0) first_last_wave_tile = 0;
+  long long r = first_last_wave_tile / kWorld;
+  return r < regions ? r : regions;
+}
+
+// Reduce items of a run: `splits` per 128-row block, 32 (4-row items) per
+// block of a tail region.
+long long items_of(long long blocks, int blocks_per_region, long long tail_region, int splits) {
+  const long long tail_blocks = blocks - tail_region * blocks_per_region;
+  return (blocks - tail_blocks) * splits + tail_blocks * (kBM / 4);
+}
+
 const void* gemm_kernel(bool fused, int pair) {
   if (pair == 2)
     return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 2>)
@@ -106,11 +125,10 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, b
   cfg->blockDim = dim3((unsigned)threads);
   cfg->dynamicSmemBytes = (size_t)gemm_smem(pair);
   cfg->stream = st;
+  // No co-residency is needed: GEMM tiles are claimed from an atomic ticket
+  // by whichever CTAs run, and producers never wait for reducers.
+  (void)fused;
   int n = 0;
-  // Reducer warps wait on tiles of other CTAs: all CTAs must be co-resident.
-  attr[n].id = cudaLaunchAttributeCooperative;
-  attr[n].val.cooperative = fused ? 1 : 0;
-  ++n;
   if (pair == 2) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = 2;
@@ -173,9 +191,10 @@ struct gemm_rs_plan_s {
   gemm_rs_desc d;
   int device = 0, num_sms = 0;
   int pair = 2, tile_rows = 256;
-  int grid = 0, reducer_warps = 0, band = 1, unit_rows = 16, units_per_region = 16;
+  int grid = 0, reducer_warps = 0, band = 1, unit_rows = 16, splits = 8, blocks_per_region = 2;
+  long long tail_region = 0;
   int mt = 0, nt = 0, num_kb = 0;
-  long long tiles = 0, units = 0;
+  long long tiles = 0, items = 0;
   Layout lay;
   uint32_t epoch = 0;
   void* last_ws = nullptr;
@@ -200,6 +219,8 @@ const char* gemm_rs_strerror(int code) {
     case GEMM_RS_ERR_WORKSPACE: return "workspace missing";
     case GEMM_RS_ERR_TOO_LARGE:
       return "problem larger than the static scratch of the no-allocation entry point";
+    case GEMM_RS_ERR_INCOMPLETE:
+      return "a fused run ended with output blocks whose 8 partials never all arrived";
     default: return "unknown status";
   }
 }
@@ -264,9 +285,12 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
                           : auto_band(d->M, d->K, h->tile_rows);
   if (h->band < 1) h->band = 1;
   h->unit_rows = d->unit_rows > 0 ? d->unit_rows : kDefaultUnitRows;
-  h->units_per_region = h->tile_rows / h->unit_rows;
-  h->units = (long long)h->mt * h->nt * h->units_per_region;
-  h->lay = layout_for(d->M, d->N, h->mt, h->nt);
+  h->splits = kBM / h->unit_rows;
+  h->blocks_per_region = h->tile_rows / kBM;
+  const long long blocks = (long long)h->mt * h->nt * h->blocks_per_region;
+  h->tail_region = tail_region_of(h->tiles, h->grid / pair, (long long)h->mt * h->nt);
+  h->items = items_of(blocks, h->blocks_per_region, h->tail_region, h->splits);
+  h->lay = layout_for(d->M, d->N, blocks, h->items);
   if (h->d.timeout_ns == 0) h->d.timeout_ns = kDefaultTimeoutNs;
   if (workspace_bytes) *workspace_bytes = h->lay.total;
   *plan = h;
@@ -286,7 +310,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->mt = h->mt;
   info->nt = h->nt;
   info->tiles = h->tiles;
-  info->units = h->units;
+  info->units = h->items;
   info->workspace_bytes = (int64_t)h->lay.total;
   info->staging_bytes = (int64_t)h->lay.staging_bytes;
   const bool empty = h->d.M == 0 || h->d.N == 0;
@@ -296,6 +320,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->launches[GEMM_RS_RS_ONLY] = empty ? 0 : 1;
   info->mma_ctas = h->pair;
   info->tile_rows = h->tile_rows;
+  info->trace_offset = (int64_t)h->lay.trace_off;
   return GEMM_RS_OK;
 }
 
@@ -383,6 +408,7 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
       return GEMM_RS_ERR_CUDA;
     p.stage = reinterpret_cast<const uint16_t*>(wsb);
     p.flags = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
+    p.queue = reinterpret_cast<unsigned long long*>(wsb + h->lay.queue_off);
     p.ctrl = reinterpret_cast<uint32_t*>(wsb + h->lay.ctrl_off);
     p.M = (int)d.M;
     p.N = (int)d.N;
@@ -392,12 +418,17 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     p.band = h->band;
     p.num_kb = h->num_kb;
     p.unit_rows = h->unit_rows;
-    p.units_per_region = h->units_per_region;
+    p.splits = h->splits;
+    p.blocks_per_region = h->blocks_per_region;
+    p.tail_region = (int)h->tail_region;
     p.tile_rows = h->tile_rows;
     p.num_tiles = h->tiles;
-    p.num_units = h->units;
+    p.num_items = h->items;
     p.debug_flags = d.debug_flags;
     p.timeout_ns = d.timeout_ns;
+    p.trace = (d.debug_flags & GEMM_RS_DEBUG_TRACE)
+                  ? reinterpret_cast<unsigned long long*>(wsb + h->lay.trace_off)
+                  : nullptr;
     h->map_A = a;
     h->map_W = w;
     h->map_ws = ws;
@@ -410,7 +441,8 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     case GEMM_RS_FUSED:
       h->params.staging_in_l2 = (d.N % 64 == 0) && !(d.debug_flags & GEMM_RS_DEBUG_NO_STAGING_L2);
       h->epoch += 1;
-      h->params.flag_target = (uint32_t)(kEpiWarps * h->pair) * h->epoch;
+      h->params.epoch = h->epoch;
+      h->params.flag_target = (uint32_t)kWorld * h->epoch;  // every rank adds 1 per block
       rc = launch_gemm(h, true, st);
       break;
     case GEMM_RS_UNFUSED:
@@ -438,7 +470,7 @@ int gemm_rs_status(gemm_rs_t h, void* stream) {
     return GEMM_RS_ERR_CUDA;
   }
   if (!h->last_ws) return GEMM_RS_OK;
-  uint32_t words[kCtrlWords];
+  static thread_local uint32_t words[kCtrlWords];
   uint8_t* wsb = static_cast<uint8_t*>(h->last_ws);
   if (cudaMemcpyAsync(words, wsb + h->lay.ctrl_off, sizeof(words), cudaMemcpyDeviceToHost, st) !=
           cudaSuccess ||
@@ -446,7 +478,8 @@ int gemm_rs_status(gemm_rs_t h, void* stream) {
     cudaGetLastError();
     return GEMM_RS_ERR_CUDA;
   }
-  if (words[kCtrlError] == 0) return GEMM_RS_OK;
+  const uint32_t err = words[kCtrlError * kCtrlStride];
+  if (err == 0) return GEMM_RS_OK;
   // Start clean: zero flags and control words, restart the epoch.
   if (cudaMemsetAsync(wsb + h->lay.flags_off, 0, h->lay.total - h->lay.flags_off, st) !=
           cudaSuccess ||
@@ -455,7 +488,8 @@ int gemm_rs_status(gemm_rs_t h, void* stream) {
     return GEMM_RS_ERR_CUDA;
   }
   h->epoch = 0;
-  return GEMM_RS_ERR_TIMEOUT;
+  return (err & (kErrFlagTimeout | kErrPipeTimeout)) ? GEMM_RS_ERR_TIMEOUT
+                                                                    : GEMM_RS_ERR_INCOMPLETE;
 }
 
 }  // extern "C"
@@ -502,8 +536,8 @@ extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const
 // cudaGetSymbolAddress while that device is current and keeps it.
 namespace {
 constexpr size_t kNoallocStagingBytes = (size_t)32 << 20;  // 8*M*N*2 <= 32 MiB
-constexpr size_t kNoallocFlagBytes = (size_t)64 << 10;     // 8*regions*4 <= 64 KiB
-constexpr size_t kNoallocCtrlBytes = 256;
+constexpr size_t kNoallocFlagBytes = (size_t)4 << 20;      // completion counts + item FIFO
+constexpr size_t kNoallocCtrlBytes = (size_t)kCtrlWords * 4;
 constexpr size_t kNoallocBytes = kNoallocStagingBytes + kNoallocFlagBytes + kNoallocCtrlBytes;
 constexpr int kNoallocMaxDevices = 64;
 }  // namespace
@@ -559,7 +593,10 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
   const int tile_rows = kBM * kDefaultMmaCtas;
   const int64_t mt = (M + tile_rows - 1) / tile_rows, nt = (N + kBN - 1) / kBN;
   const size_t staging = (size_t)kWorld * (size_t)M * (size_t)N * 2;
-  const size_t flag_bytes = (size_t)kWorld * (size_t)mt * (size_t)nt * 4;
+  const int64_t blocks = mt * nt * (tile_rows / kBM);
+  const int64_t items = blocks * (kBM / 4);  // at most 32 items per block
+  const size_t count_bytes = (size_t)blocks * kFlagStride * 4;
+  const size_t flag_bytes = align_up(count_bytes, 256) + (size_t)items * kQueueStride * 8;
   if (staging > kNoallocStagingBytes || flag_bytes > kNoallocFlagBytes) return GEMM_RS_ERR_TOO_LARGE;
   const bool empty = M == 0 || N == 0;
   if (!empty && (!out || (K > 0 && (!A || !W)))) return GEMM_RS_ERR_INVALID_ARG;
@@ -607,6 +644,9 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.stage = reinterpret_cast<const uint16_t*>(scratch);
     p.out = static_cast<uint16_t*>(out);
     p.flags = flags;
+    p.queue = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(flags) +
+                                                    align_up(count_bytes, 256));
+    p.epoch = 1;  // the FIFO slots were just cleared (tag 0)
     p.ctrl = ctrl;
     p.M = (int)M;
     p.N = (int)N;
@@ -616,18 +656,20 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.band = auto_band(M, K, tile_rows);
     p.num_kb = (int)((Kr + kBK - 1) / kBK);
     p.unit_rows = kDefaultUnitRows;
-    p.units_per_region = tile_rows / kDefaultUnitRows;
+    p.splits = kBM / kDefaultUnitRows;
+    p.blocks_per_region = tile_rows / kBM;
     p.tile_rows = tile_rows;
     p.num_tiles = (long long)kWorld * mt * nt;
-    p.num_units = (long long)mt * nt * p.units_per_region;
-    // flags were just cleared: one run's worth of adds
-    p.flag_target = (uint32_t)(kEpiWarps * kDefaultMmaCtas);
+    const long long tail = tail_region_of(p.num_tiles, nd->grid / kDefaultMmaCtas, mt * nt);
+    p.tail_region = (int)tail;
+    p.num_items = items_of(blocks, p.blocks_per_region, tail, p.splits);
+    p.flag_target = (uint32_t)kWorld;  // counts were just cleared: one run's worth of adds
     p.timeout_ns = kDefaultTimeoutNs;
     rc = launch_gemm_kernel(kDefaultMmaCtas, true, nd->grid,
                             32 * (kGemmWarps + kDefaultReducerWarps), p, st);
     if (rc != GEMM_RS_OK) return rc;
   }
-  if (error_word && cudaMemcpyAsync(error_word, ctrl + kCtrlError, sizeof(uint32_t),
+  if (error_word && cudaMemcpyAsync(error_word, ctrl + kCtrlError * kCtrlStride, sizeof(uint32_t),
                                     cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_RS_ERR_CUDA;

@@ -20,12 +20,16 @@
 //                 (bf16 in, fp32 in TMEM, two 256-column accumulators);
 //                 TMEM allocation in every CTA
 //   warps 2..5    epilogue: TMEM -> registers -> bf16 (RNE) -> swizzled smem ->
-//                 TMA store into the rank's staging region; then the tile's
-//                 flag is raised with a release add (fused kernel only)
-//   warps 6..     reducers (fused kernel only): claim reduce units in tile
-//                 order, acquire the 8 rank flags of the unit's region, add the
-//                 8 bf16 partials in fp32 in rank order, write bf16 output.
-//                 The epilogue warps join them when the CTA's tiles are done.
+//                 TMA store into the rank's staging region; then (fused kernel)
+//                 once the 4 warps' stores of the CTA's 128 rows of a tile
+//                 have landed, one thread publishes them with a release add on
+//                 that 128-row block's completion count; the rank tile that
+//                 completes a block (the 8th add) appends the block's reduce
+//                 items to a global FIFO
+//   warps 6..     reducers (fused kernel only): take the next FIFO position,
+//                 wait (acquire) until its item is there, add the 8 bf16
+//                 partials in fp32 in rank order, write bf16 output.  The
+//                 epilogue warps join them when the CTA's tiles are done.
 // Every wait is bounded by p.timeout_ns; on expiry the kernel records an error
 // word, stops its loops, lets its in-flight copies land, frees TMEM and returns.
 #pragma once
@@ -38,7 +42,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16 columns
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
-constexpr int kMaxReducerWarps = 8;
+constexpr int kMaxReducerWarps = 6;
 
 // Shared-memory plan of one CTA for 1 or 2 CTAs per MMA.
 template <int kPair>
@@ -55,9 +59,11 @@ struct TileCfg {
   static constexpr int kSmemB = kSmemA + kStages * kAStage;
   static constexpr int kSmemEpi = kSmemB + kStages * kBStage;
   static constexpr int kSmemBar = kSmemEpi + kEpiWarps * 2 * kEpiBufBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;   // full, empty, acc_full[2], acc_empty[2], drain
+  // full[S], empty[S], acc_full[2], acc_empty[2], drain, tile ring full[4], empty[4]
+  static constexpr int kNumBars = 2 * kStages + 5 + 2 * 4;
   static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kSmemMisc + 16;
+  // tmem addr, abort, items reduced, pad, ring slots[4], tiles landed per epilogue warp[4]
+  static constexpr int kSmemBytes = kSmemMisc + 16 + 4 * 4 + 4 * kEpiWarps;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack to align the base to 1024 bytes
   static constexpr uint32_t kFlagAddsPerTile = kEpiWarps * kPair;
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
@@ -65,15 +71,24 @@ struct TileCfg {
 
 // control words in the workspace
 enum CtrlWord : int {
-  kCtrlTicket = 0,   // next reduce unit to claim
+  kCtrlReduced = 0,  // reduce items finished in this run (checked by the last CTA)
+  kCtrlQueueTail = 7,  // next FIFO position to fill
+  kCtrlQueueHead = 8,  // next FIFO position to take
   kCtrlDone = 1,     // CTAs finished (the last one resets the words above and below)
   kCtrlAbort = 2,    // set when some warp gave up waiting
   kCtrlError = 3,    // error bits (kErr*), cleared by the host
   kCtrlErrWhere = 4, // which wait gave up
   kCtrlErrWhat = 5,  // region / tile index of that wait
-  kCtrlWords = 16
+  kCtrlTileTicket = 6, // next GEMM tile to claim
+  kCtrlCount = 16
 };
-enum ErrBits : uint32_t { kErrFlagTimeout = 1u, kErrPipeTimeout = 2u };
+// Every control word, completion count and FIFO slot sits in its own part of
+// a cache line, so atomics and polls on one do not queue behind another's.
+constexpr int kCtrlStride = 32;   // words: one 128-byte line per control word
+constexpr int kCtrlWords = kCtrlCount * kCtrlStride;
+constexpr int kFlagStride = 32;   // words: one 128-byte line per block count
+constexpr int kQueueStride = 4;   // 8-byte slots: one 32-byte sector per slot
+enum ErrBits : uint32_t { kErrFlagTimeout = 1u, kErrPipeTimeout = 2u, kErrIncomplete = 4u };
 enum ErrWhere : uint32_t { kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereReducer = 4 };
 
 struct GemmParams {
@@ -82,14 +97,27 @@ struct GemmParams {
   CUtensorMap tmap_st;  // staging [8][M][N] : dims {N, M, 8}, box {64, 32, 1}
   const uint16_t* stage;
   uint16_t* out;
-  uint32_t* flags;  // [8][mt_count * nt_count]; each tile adds kFlagAddsPerTile per fused run
-  uint32_t* ctrl;   // kCtrlWords words
+  // Completion count per 128-row block of the output (a region's blocks are
+  // consecutive, one per CTA of the pair): every rank's tile adds 1 per fused
+  // run, so a run's target is 8 * (runs so far) and the add that reaches it
+  // completes the block.
+  uint32_t* flags;
+  uint32_t* ctrl;   // kCtrlWords words (kCtrlCount words, kCtrlStride apart)
   int M, N, Kr;
   int mt_count, nt_count, band;  // mt_count and band count tile rows of kTileRows rows
   int num_kb;
-  int unit_rows, units_per_region;
+  int unit_rows;          // rows per reduce item: 8, 16 or 32
+  int splits;             // reduce items per 128-row block (128 / unit_rows)
+  int blocks_per_region;  // tile_rows / 128
+  // Regions from tail_region on are completed by the last wave of tiles: their
+  // blocks are cut into 4-row items so the reduction after the last tile is
+  // spread over many warps.  An item is (block << 5) | part.
+  int tail_region;
   long long num_tiles;
-  long long num_units;
+  long long num_items;    // reduce items of a run
+  // FIFO of reduce items, one slot per item of a run: slot = (epoch << 32) | item
+  unsigned long long* queue;
+  uint32_t epoch;         // fused runs on this workspace so far, this one included
   uint32_t flag_target;
   uint32_t debug_flags;
   // Fused kernel only: staging tiles are stored with an L2 evict-last hint so
@@ -99,16 +127,21 @@ struct GemmParams {
   uint32_t staging_in_l2;
   int tile_rows;  // rows of a region: 128 (one CTA per MMA) or 256 (a CTA pair)
   unsigned long long timeout_ns;
+  // Debug timeline (null unless asked for): per CTA, global-timer stamps
+  // [start, epilogue done with its tiles, MMA issue drained, last warp done].
+  unsigned long long* trace;
 };
+constexpr int kTraceWords = 4;
+constexpr int kMaxTraceCtas = 1024;
 
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void record_error(const GemmParams& p, uint32_t bit, uint32_t where,
                                              uint32_t what) {
-  atomicOr(p.ctrl + kCtrlError, bit);
-  atomicExch(p.ctrl + kCtrlErrWhere, where);
-  atomicExch(p.ctrl + kCtrlErrWhat, what);
-  atomicExch(p.ctrl + kCtrlAbort, 1u);
+  atomicOr(p.ctrl + kCtrlError * kCtrlStride, bit);
+  atomicExch(p.ctrl + kCtrlErrWhere * kCtrlStride, where);
+  atomicExch(p.ctrl + kCtrlErrWhat * kCtrlStride, what);
+  atomicExch(p.ctrl + kCtrlAbort * kCtrlStride, 1u);
 }
 
 // Bounded mbarrier wait; false if the limit passed or the CTA is aborting.
@@ -153,100 +186,222 @@ __device__ __forceinline__ uint4 reduce8(const uint4 (&v)[kWorld]) {
   return o;
 }
 
-// Wait (bounded) until the 8 rank tiles of `region` are published for this
-// run.  Every lane performs its own acquire loads of all 8 flags, so each
-// lane's later staging loads are ordered after the producers' releases.
-__device__ __forceinline__ bool wait_region_flags(const GemmParams& p, int region, int lane) {
-  const size_t regions = (size_t)p.mt_count * p.nt_count;
-  const uint32_t* f = p.flags + region;
+// Append the items (block << 5) | 0..parts-1 to the global FIFO.  Called by
+// the thread whose add completed the block, right after its acquire-release
+// fence: the fence plus these relaxed stores release the block to whoever
+// acquires a slot.  One add reserves all the positions.
+__device__ __forceinline__ void queue_push_block(const GemmParams& p, int block, int parts) {
+  const uint32_t pos = atomicAdd(p.ctrl + kCtrlQueueTail * kCtrlStride, (uint32_t)parts);
+  for (int sp = 0; sp < parts; ++sp)
+    st_relaxed_gpu_u64(p.queue + (size_t)(pos + sp) * kQueueStride,
+                       ((uint64_t)p.epoch << 32) | (uint32_t)((block << 5) | sp));
+}
+
+// Take the next FIFO position and wait for its item: the item, -1 when every
+// item of the run is taken, -2 if the wait gave up.  Every lane acquires the
+// filled slot itself, so each lane's loads of the staging are ordered after
+// the releases that completed the block.
+__device__ __forceinline__ int queue_pop(const GemmParams& p, int lane) {
+  uint32_t pos = 0;
+  if (lane == 0) pos = atomicAdd(p.ctrl + kCtrlQueueHead * kCtrlStride, 1u);
+  pos = __shfl_sync(0xffffffffu, pos, 0);
+  if ((long long)pos >= p.num_items) return -1;
+  const unsigned long long* slot = p.queue + (size_t)pos * kQueueStride;
   uint64_t t0 = 0;
   if (lane == 0) t0 = globaltimer_ns();
   uint32_t sleep_ns = 64;
   while (true) {
-    bool ok = true;
-#pragma unroll
-    for (int r = 0; r < kWorld; ++r) {
-      const uint32_t v = ld_acquire_gpu(f + (size_t)r * regions);
-      ok = ok && ((int32_t)(v - p.flag_target) >= 0);
+    // poll with relaxed loads (an acquire per poll would cost every waiting
+    // warp an L1 invalidation); acquire once the slot is filled
+    int ready = 0;
+    if (lane == 0) ready = (uint32_t)(ld_relaxed_gpu_u64(slot) >> 32) == p.epoch;
+    if (__shfl_sync(0xffffffffu, ready, 0)) {
+      const uint64_t v = ld_acquire_gpu_u64(slot);
+      return (int)(uint32_t)v;
     }
-    if (__all_sync(0xffffffffu, ok)) return true;
     int give_up = 0;
     if (lane == 0)
-      give_up = (globaltimer_ns() - t0 > p.timeout_ns) || ld_volatile_u32(p.ctrl + kCtrlAbort);
-    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+      give_up = (globaltimer_ns() - t0 > p.timeout_ns) || ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride);
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return -2;
     __nanosleep(sleep_ns);
     sleep_ns = sleep_ns < 1024 ? sleep_ns * 2 : 1024;
   }
 }
 
-// Drop the staging lines of one output row segment from L2 (fused kernel,
-// after the whole warp has consumed them).
-__device__ __forceinline__ void discard_row(const GemmParams& p, size_t plane, size_t off,
-                                            int lane) {
-  if ((lane & 7) == 0) {
+// Rows [row, row + R) of one reduce item: 8R loads of 16 bytes in flight per
+// lane, then the rank-order sums and the stores.
+template <int R>
+__device__ __forceinline__ void reduce_rows(const GemmParams& p, size_t plane, int row, int col,
+                                            bool active, bool drop) {
+  const size_t off = (size_t)row * p.N + col;
+  if (active) {
+    uint4 v[R][kWorld];
 #pragma unroll
-    for (int r = 0; r < kWorld; ++r) discard_l2_line(p.stage + r * plane + off);
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int r = 0; r < kWorld; ++r)
+        v[i][r] = __ldcg(reinterpret_cast<const uint4*>(p.stage + r * plane + off + (size_t)i * p.N));
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      *reinterpret_cast<uint4*>(p.out + off + (size_t)i * p.N) = reduce8(v[i]);
+  }
+  if (p.staging_in_l2) {
+    __syncwarp();  // every lane has consumed its loads (its stores depend on them)
+    if (drop) {
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int r = 0; r < kWorld; ++r)
+          discard_l2_line(p.stage + r * plane + off + (size_t)i * p.N);
+    }
   }
 }
 
-// Reducer role: claim units until none are left.  A unit is unit_rows rows x
-// 256 columns of one region; lane l covers columns [8l, 8l+8) of it.
-__device__ __noinline__ void reducer_loop(const GemmParams& p, int lane) {
+// Reduce one item of a completed 128-row block (lane l covers columns
+// [8l, 8l+8) of the block's 256).  With p.staging_in_l2 the staging lines
+// just read are dropped from L2.
+__device__ __forceinline__ void reduce_item(const GemmParams& p, int item, int lane) {
   const size_t plane = (size_t)p.M * p.N;
+  const int block = item >> 5;
+  const int part = item & 31;
+  const int region = block / p.blocks_per_region;
+  const int rb = block - region * p.blocks_per_region;
+  const int mt = region / p.nt_count;
+  const int nt = region - mt * p.nt_count;
+  const int rows = region >= p.tail_region ? 4 : p.unit_rows;
+  const int row_begin = mt * p.tile_rows + rb * kBM + part * rows;
+  if (row_begin >= p.M) return;  // rows of a ragged last tile that do not exist
+  int row_end = row_begin + rows;
+  if (row_end > p.M) row_end = p.M;
+  const int col = nt * kBN + lane * 8;
+  const bool active = col < p.N;
+  const bool drop = p.staging_in_l2 && active && (lane & 7) == 0;
+  int row = row_begin;
+#pragma unroll 1
+  for (; row + 3 < row_end; row += 4) reduce_rows<4>(p, plane, row, col, active, drop);
+  if (row + 1 < row_end) {
+    reduce_rows<2>(p, plane, row, col, active, drop);
+    row += 2;
+  }
+  if (row < row_end) reduce_rows<1>(p, plane, row, col, active, drop);
+}
+
+// Reducer role: take FIFO positions until every item of the run is taken.
+// Items done are counted in the CTA's shared counter (added to the run's
+// total once, when the CTA ends).
+__device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_t* cta_reduced) {
   while (true) {
-    uint32_t u = 0;
-    if (lane == 0) u = atomicAdd(p.ctrl + kCtrlTicket, 1u);
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if ((long long)u >= p.num_units) break;
-    const int pos = (int)(u / (uint32_t)p.units_per_region);
-    const int sub = (int)(u - (uint32_t)pos * (uint32_t)p.units_per_region);
-    const Region g = region_at(pos, p.mt_count, p.nt_count, p.band);
-    const int region = g.mt * p.nt_count + g.nt;
-    const int row_begin = g.mt * p.tile_rows + sub * p.unit_rows;
-    if (row_begin >= p.M) continue;  // rows of a ragged last tile that do not exist
-    if (!wait_region_flags(p, region, lane)) {
-      if (lane == 0 && !ld_volatile_u32(p.ctrl + kCtrlAbort))
-        record_error(p, kErrFlagTimeout, kWhereReducer, (uint32_t)region);
+    const int item = queue_pop(p, lane);
+    if (item == -1) break;
+    if (item == -2) {
+      if (lane == 0 && !ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride))
+        record_error(p, kErrFlagTimeout, kWhereReducer, 0xFFFFFFFFu);
       break;
     }
-    int row_end = row_begin + p.unit_rows;
-    if (row_end > p.M) row_end = p.M;
-    const int col = g.nt * kBN + lane * 8;
-    if (col < p.N) {
-      int row = row_begin;
-#pragma unroll 1
-      for (; row + 1 < row_end; row += 2) {
-        const size_t off0 = (size_t)row * p.N + col;
-        const size_t off1 = off0 + p.N;
-        uint4 v0[kWorld], v1[kWorld];
-#pragma unroll
-        for (int r = 0; r < kWorld; ++r) {
-          v0[r] = __ldcg(reinterpret_cast<const uint4*>(p.stage + r * plane + off0));
-          v1[r] = __ldcg(reinterpret_cast<const uint4*>(p.stage + r * plane + off1));
-        }
-        *reinterpret_cast<uint4*>(p.out + off0) = reduce8(v0);
-        *reinterpret_cast<uint4*>(p.out + off1) = reduce8(v1);
-        if (p.staging_in_l2) {
-          __syncwarp();  // every lane has consumed its loads (its stores depend on them)
-          discard_row(p, plane, off0, lane);
-          discard_row(p, plane, off1, lane);
-        }
-      }
-      if (row < row_end) {
-        const size_t off0 = (size_t)row * p.N + col;
-        uint4 v0[kWorld];
-#pragma unroll
-        for (int r = 0; r < kWorld; ++r)
-          v0[r] = __ldcg(reinterpret_cast<const uint4*>(p.stage + r * plane + off0));
-        *reinterpret_cast<uint4*>(p.out + off0) = reduce8(v0);
-        if (p.staging_in_l2) {
-          __syncwarp();
-          discard_row(p, plane, off0, lane);
-        }
-      }
-    }
+    reduce_item(p, item, lane);
+    __syncwarp();
+    if (lane == 0) atomicAdd(cta_reduced, 1u);
   }
 }
+
+// Wait until at most n bulk groups of this thread are incomplete.
+__device__ __forceinline__ void bulk_wait_upto(int n) {
+  switch (n) {
+    case 0: bulk_wait_all<0>(); break;
+    case 1: bulk_wait_all<1>(); break;
+    case 2: bulk_wait_all<2>(); break;
+    case 3: bulk_wait_all<3>(); break;
+    default: bulk_wait_all<4>(); break;
+  }
+}
+
+// One rank's 128-row block of a tile is in global memory (all 4 epilogue
+// warps' stores landed and were fenced, then met on an smem barrier): count
+// it with a release add and, if it is the 8th rank, acquire the others and
+// queue the block's items.
+__device__ __forceinline__ void publish_block(const GemmParams& p, int block, bool skip) {
+  if (skip) return;  // debug: this completion never arrives
+  const uint32_t old = atom_add_release_gpu(p.flags + (size_t)block * kFlagStride, 1u);
+  if (old == p.flag_target - 1u) {
+    fence_acq_rel_gpu();  // acquire the other ranks' releases, release to the FIFO
+    const int region = block / p.blocks_per_region;
+    queue_push_block(p, block, region >= p.tail_region ? kBM / 4 : p.splits);
+  }
+}
+
+// Epilogue warp `ew` has its rows of the n-th published tile in global memory
+// (stores complete and proxy-fenced): record it; warp 0 then waits until all
+// 4 warps recorded tile n and publishes the CTA's 128-row block once.
+__device__ __forceinline__ void land_and_publish(const GemmParams& p, volatile uint32_t* landed,
+                                                 int ew, int n, int block, bool skip,
+                                                 uint64_t limit, volatile uint32_t* cta_abort) {
+  __threadfence_block();
+  landed[ew] = (uint32_t)n;
+  if (ew != 0) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (int w = 1; w < kEpiWarps; ++w) {
+    while ((int)(landed[w] - (uint32_t)n) < 0) {
+      if (*cta_abort || globaltimer_ns() - t0 > limit) {
+        if (!*cta_abort) {
+          record_error(p, kErrPipeTimeout, kWhereEpi, (uint32_t)block);
+          *cta_abort = 1;
+        }
+        return;
+      }
+      __nanosleep(32);
+    }
+  }
+  __threadfence_block();
+  publish_block(p, block, skip);
+}
+
+// ---------------------------------------------------------------------------
+// Tile ring: the pair leader's TMA thread claims rank tiles from one atomic
+// ticket (so no tile waits for a CTA that is not running) and hands each tile
+// index to every consumer through a small ring in shared memory, mirrored
+// into the peer CTA.  Consumers: the MMA thread (leader), the 4 epilogue
+// warps of each CTA and, in a pair, the peer's TMA thread.  Index -1 ends the
+// stream.
+template <int kPair>
+struct TileRing {
+  static constexpr int kDepth = 4;
+  static constexpr uint32_t kConsumers = kPair == 1 ? 1 + kEpiWarps : 2 + 2 * kEpiWarps;
+  uint32_t slots;   // shared address of int32 slot[kDepth]
+  uint32_t full;    // shared address of mbarrier full[kDepth]
+  uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in the leader)
+  int slot = 0;
+  uint32_t phase = 0;
+
+  __device__ __forceinline__ void advance() {
+    if (++slot == kDepth) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  // Producer (leader TMA thread): publish the next claimed tile, or -1.
+  __device__ __forceinline__ bool put(int tile, uint64_t limit, volatile uint32_t* abort) {
+    if (!bar_wait<kPair == 2>(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
+    st_shared_u32(slots + 4 * slot, (uint32_t)tile);
+    mbar_arrive(full + 8 * slot);
+    if constexpr (kPair == 2) {
+      st_shared_cluster_u32(mapa_shared(slots + 4 * slot, 1), (uint32_t)tile);
+      mbar_arrive_cluster(mapa_shared(full + 8 * slot, 1));
+    }
+    advance();
+    return true;
+  }
+  // Consumer: next tile index (-1 at the end); false if the wait gave up.
+  __device__ __forceinline__ bool get(int* tile, uint64_t limit, volatile uint32_t* abort) {
+    if (!bar_wait<kPair == 2>(full + 8 * slot, phase, limit, abort)) return false;
+    *tile = (int)ld_shared_u32(slots + 4 * slot);
+    if constexpr (kPair == 2)
+      mbar_arrive_cluster(mapa_shared(empty + 8 * slot, 0));
+    else
+      mbar_arrive(empty + 8 * slot);
+    advance();
+    return true;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // The persistent GEMM kernel.  kFused = true adds flags and reducer warps;
@@ -255,6 +410,7 @@ template <bool kFused, int kPair>
 __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps : 0)), 1)
     gemm_rs_kernel(const __grid_constant__ GemmParams p) {
   using C = TileCfg<kPair>;
+  using Ring = TileRing<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -262,16 +418,20 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   const int lane = threadIdx.x & 31;
   const uint32_t cta_rank = kPair == 2 ? cluster_ctarank() : 0u;
   const bool leader = cta_rank == 0;
-  const long long first_tile = blockIdx.x / kPair;
-  const long long tile_step = gridDim.x / kPair;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::kSmemBar;
   const uint32_t bar_empty = bar_full + 8 * C::kStages;
   const uint32_t bar_acc_full = bar_empty + 8 * C::kStages;
   const uint32_t bar_acc_empty = bar_acc_full + 16;
   const uint32_t bar_drain = bar_acc_empty + 16;
+  const uint32_t bar_ring_full = bar_drain + 8;
+  const uint32_t bar_ring_empty = bar_ring_full + 8 * Ring::kDepth;
+  // tiles whose stores have landed, per epilogue warp (monotonic counts)
+  volatile uint32_t* landed = reinterpret_cast<volatile uint32_t*>(smem + C::kSmemMisc + 32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
   volatile uint32_t* cta_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kSmemMisc + 4);
+  uint32_t* cta_reduced = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc + 8);
+  const uint32_t ring_slots = sbase + C::kSmemMisc + 16;
   const uint64_t limit = p.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -284,7 +444,13 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       mbar_init(bar_acc_empty + 8 * b, kEpiWarps * kPair);  // every epilogue warp of the pair
     }
     mbar_init(bar_drain, 1);
+    for (int s = 0; s < Ring::kDepth; ++s) {
+      mbar_init(bar_ring_full + 8 * s, 1);
+      mbar_init(bar_ring_empty + 8 * s, Ring::kConsumers);
+    }
+    for (int w = 0; w < kEpiWarps; ++w) landed[w] = 0;
     *cta_abort = 0;
+    *cta_reduced = 0;
     fence_mbar_init();
     fence_proxy_async_shared();
     tma_prefetch_desc(&p.tmap_a);
@@ -300,14 +466,34 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   if constexpr (kPair == 2) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  unsigned long long* trace =
+      (p.trace && blockIdx.x < kMaxTraceCtas) ? p.trace + blockIdx.x * kTraceWords : nullptr;
+  if (trace && threadIdx.x == 0) trace[0] = globaltimer_ns();
+  Ring ring{ring_slots, bar_ring_full, bar_ring_empty};
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, issued_par = 0;
-      bool ok = true;
-      for (long long idx = first_tile; ok && idx < p.num_tiles; idx += tile_step) {
+      while (true) {
+        int idx = -1;
+        bool ok;
+        if (leader) {  // claim the next tile for the pair and publish it
+          const uint32_t t = atomicAdd(p.ctrl + kCtrlTileTicket * kCtrlStride, 1u);
+          idx = (long long)t < p.num_tiles ? (int)t : -1;
+          ok = ring.put(idx, limit, cta_abort);
+        } else {
+          ok = ring.get(&idx, limit, cta_abort);
+        }
+        if (!ok) {
+          if (!*cta_abort) {
+            record_error(p, kErrPipeTimeout, kWhereTma, 0xFFFFFFFFu);
+            *cta_abort = 1;
+          }
+          break;
+        }
+        if (idx < 0) break;
         const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
         const int m0 = tc.mt * C::kTileRows + (int)cta_rank * kBM;
         const int n0 = tc.nt * kBN + (int)cta_rank * C::kBCols;
@@ -346,6 +532,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             phase ^= 1u;
           }
         }
+        if (!ok) break;
       }
       // Let every copy this thread started land before the CTA can exit (the
       // leader's barriers also count the peer's bytes).
@@ -362,7 +549,16 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (long long idx = first_tile; ok && idx < p.num_tiles; idx += tile_step) {
+      while (ok) {
+        int idx = -1;
+        if (!ring.get(&idx, limit, cta_abort)) {
+          if (!*cta_abort) {
+            record_error(p, kErrPipeTimeout, kWhereMma, 0xFFFFFFFFu);
+            *cta_abort = 1;
+          }
+          break;
+        }
+        if (idx < 0) break;
         if (!bar_wait<kPair == 2>(bar_acc_empty + 8 * acc, acc_phase ^ 1u, limit, cta_abort)) {
           if (!*cta_abort) {
             record_error(p, kErrPipeTimeout, kWhereMma, (uint32_t)idx);
@@ -416,6 +612,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       // All MMAs of this thread complete before TMEM can be released.
       mma_commit<kPair>(bar_drain);
       bar_wait(bar_drain, 0, limit, cta_abort);
+      if (trace) trace[2] = globaltimer_ns();
     }
     __syncwarp();
   } else if (warp < kGemmWarps) {
@@ -424,16 +621,23 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
     const int ew = warp - 2;
     const uint32_t buf_s = sbase + C::kSmemEpi + ew * 2 * kEpiBufBytes;
     uint8_t* buf_p = smem + C::kSmemEpi + ew * 2 * kEpiBufBytes;
-    const size_t regions = (size_t)p.mt_count * p.nt_count;
     const bool hint = kFused && p.staging_in_l2;
     const uint64_t keep_policy = hint ? policy_evict_last() : 0;
     int acc = 0, buf = 0;
     uint32_t acc_phase = 0;
-    for (long long idx = first_tile; idx < p.num_tiles; idx += tile_step) {
-      const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
-      int got = 0;
-      if (lane == 0) got = bar_wait(bar_acc_full + 8 * acc, acc_phase, limit, cta_abort);
+    int pend_block = -1;     // block of the previous tile, published one tile late
+    bool pend_skip = false;
+    int pend_n = 0;          // tiles published so far (landed-barrier phase)
+    while (true) {
+      int idx = -1, got = 0;
+      if (lane == 0) {
+        got = ring.get(&idx, limit, cta_abort) ? 1 : 0;
+        if (got && idx >= 0)
+          got = bar_wait(bar_acc_full + 8 * acc, acc_phase, limit, cta_abort) ? 1 : 0;
+      }
       got = __shfl_sync(0xffffffffu, got, 0);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (lane != 0) ring.advance();  // keep every lane's ring position in step
       if (!got) {
         if (lane == 0 && !*cta_abort) {
           record_error(p, kErrPipeTimeout, kWhereEpi, (uint32_t)idx);
@@ -441,9 +645,12 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
         }
         break;
       }
+      if (idx < 0) break;
+      const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
       tc_fence_after();
       const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32;
       const bool rows_in = row0 < p.M;
+      int groups = 0;  // bulk groups this tile commits (lane 0)
 #pragma unroll 1
       for (int c = 0; c < kBN / 64; ++c) {
         uint32_t v0[32], v1[32];
@@ -489,33 +696,46 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             else
               tma_store_3d(&p.tmap_st, buf_s + buf * kEpiBufBytes, col0, row0, tc.rank);
             bulk_commit();
+            ++groups;
           }
           buf ^= 1;
         }
       }
       if (kFused) {
+        // Publish the previous tile's block now that this tile's stores are
+        // issued: its stores have had this tile's TMEM work to complete.
         if (lane == 0) {
-          bulk_wait_all<0>();          // this warp's part of the tile is in global memory
-          fence_proxy_async_global();  // order the async-proxy writes before the release
-          const bool skip = (p.debug_flags & 1u) && idx == 0 && ew == 0 && leader;
-          if (!skip)
-            red_release_gpu_add(p.flags + (size_t)tc.rank * regions +
-                                    (size_t)tc.mt * p.nt_count + tc.nt,
-                                1u);
+          if (pend_block >= 0) {
+            bulk_wait_upto(groups);      // at most this tile's groups still in flight
+            fence_proxy_async_global();  // order the async-proxy writes before the release
+            ++pend_n;
+            land_and_publish(p, landed, ew, pend_n, pend_block, pend_skip, limit, cta_abort);
+          }
+          pend_block = ((int)(tc.mt * p.nt_count + tc.nt)) * p.blocks_per_region + (int)cta_rank;
+          pend_skip = (p.debug_flags & 1u) && idx == 0 && leader;
         }
         __syncwarp();
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait_all<0>();
+    if (lane == 0) {
+      bulk_wait_all<0>();
+      if (kFused && pend_block >= 0) {
+        fence_proxy_async_global();
+        ++pend_n;
+        land_and_publish(p, landed, ew, pend_n, pend_block, pend_skip, limit, cta_abort);
+      }
+    }
     __syncwarp();
-    if (kFused) reducer_loop(p, lane);  // out of tiles: help with the reduction
+    if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
+    if (kFused) reducer_loop(p, lane, cta_reduced);  // out of tiles: help with the reduction
   } else {
     // ------------------------------------------------------------ reducers
-    if (kFused) reducer_loop(p, lane);
+    if (kFused) reducer_loop(p, lane, cta_reduced);
   }
 
+  if (trace && lane == 0) atomicMax(trace + 3, (unsigned long long)globaltimer_ns());
   tc_fence_before();
   __syncthreads();
   if constexpr (kPair == 2) cluster_sync();  // no MMA or remote arrive targets this CTA any more
@@ -523,14 +743,19 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
     tc_fence_after();
     tmem_dealloc<kPair>(tmem_base, kTmemCols);
   }
-  if (kFused && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
+    if (kFused) atomicAdd(p.ctrl + kCtrlReduced * kCtrlStride, *cta_reduced);
     __threadfence();
-    const uint32_t prev = atomicAdd(p.ctrl + kCtrlDone, 1u);
-    if (prev == gridDim.x - 1) {  // last CTA: reset the per-run counters
+    const uint32_t prev = atomicAdd(p.ctrl + kCtrlDone * kCtrlStride, 1u);
+    if (prev == gridDim.x - 1) {  // last CTA: check the run, reset the per-run counters
       __threadfence();
-      atomicExch(p.ctrl + kCtrlTicket, 0u);
-      atomicExch(p.ctrl + kCtrlAbort, 0u);
-      atomicExch(p.ctrl + kCtrlDone, 0u);
+      if (kFused && (long long)atomicExch(p.ctrl + kCtrlReduced * kCtrlStride, 0u) != p.num_items)
+        atomicOr(p.ctrl + kCtrlError * kCtrlStride, (uint32_t)kErrIncomplete);
+      atomicExch(p.ctrl + kCtrlQueueTail * kCtrlStride, 0u);
+      atomicExch(p.ctrl + kCtrlQueueHead * kCtrlStride, 0u);
+      atomicExch(p.ctrl + kCtrlTileTicket * kCtrlStride, 0u);
+      atomicExch(p.ctrl + kCtrlAbort * kCtrlStride, 0u);
+      atomicExch(p.ctrl + kCtrlDone * kCtrlStride, 0u);
       __threadfence();
     }
   }

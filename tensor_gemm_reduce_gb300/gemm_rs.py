@@ -31,6 +31,7 @@ GEMM_RS_ERR_TIMEOUT = -5
 GEMM_RS_ERR_MISALIGNED = -6
 GEMM_RS_ERR_WORKSPACE = -7
 GEMM_RS_ERR_TOO_LARGE = -8
+GEMM_RS_ERR_INCOMPLETE = -9
 
 # Fixed scratch of the no-allocation entry point (see gemm_rs_fused_noalloc).
 NOALLOC_STAGING_BYTES = 32 << 20
@@ -40,6 +41,7 @@ MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": 
 
 DEBUG_SKIP_ONE_FLAG = 0x1
 DEBUG_NO_STAGING_L2 = 0x2
+DEBUG_TRACE = 0x4
 
 
 class gemm_rs_desc(ctypes.Structure):
@@ -76,6 +78,7 @@ class gemm_rs_info(ctypes.Structure):
         ("launches", ctypes.c_int32 * 4),
         ("mma_ctas", ctypes.c_int32),
         ("tile_rows", ctypes.c_int32),
+        ("trace_offset", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -298,6 +301,13 @@ class Plan:
         import torch
         s = stream if stream is not None else torch.cuda.current_stream()
         return gemm_rs_status(self._h, s.cuda_stream)
+
+    def trace(self, workspace):
+        """GEMM_RS_DEBUG_TRACE stamps of the last run: int64 tensor [grid][4] (ns)."""
+        import torch
+        off = self.info.trace_offset
+        n = self.info.grid * 4
+        return workspace[off: off + 8 * n].view(torch.int64).view(-1, 4).cpu()
 
     def close(self):
         if getattr(self, "_h", None):

@@ -34,9 +34,10 @@ def _create(**kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(world=4), G.GEMM_RS_ERR_INVALID_ARG),
-    (dict(reducer_warps=9), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(reducer_warps=7), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(reducer_warps=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(unit_rows=12), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(unit_rows=64), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(grid=-2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(mma_ctas=3), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
@@ -61,7 +62,7 @@ def test_null_arguments(lib):
 
 
 def test_strerror(lib):
-    for code in range(-7, 1):
+    for code in range(-9, 1):
         assert G.strerror(code) and G.strerror(code) != f"status {code}"
     assert G.strerror(-99) == "unknown status"
 
