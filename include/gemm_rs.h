@@ -89,8 +89,9 @@ typedef struct gemm_rs_desc {
   int32_t unit_rows;      /* rows per reduce item in FUSED mode: 8, 16 or 32; 0 = 16 */
   uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
   uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
-  int32_t mma_ctas;       /* CTAs per MMA tile: 1 (128 x 256 tiles) or 2 (a 2-CTA cluster
-                             computes 256 x 256 tiles); 0 = 2 */
+  int32_t mma_ctas;       /* CTAs of a cluster sharing one tile: 1 (128 x 256 tiles), 2 (a
+                             2-CTA MMA, 256 x 256 tiles) or 4 (two 2-CTA MMAs, 512 x 256
+                             tiles, W tiles shared by TMA multicast); 0 = 2 */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -110,7 +111,7 @@ typedef struct gemm_rs_info {
   int64_t workspace_bytes;
   int64_t staging_bytes;  /* 8 * M * N * 2 */
   int32_t launches[4];    /* kernels launched per gemm_rs_run, indexed by mode */
-  int32_t mma_ctas;       /* CTAs per MMA tile */
+  int32_t mma_ctas;       /* CTAs of a cluster sharing one tile */
   int32_t tile_rows;      /* output rows of one rank tile: 128 * mma_ctas */
   int64_t trace_offset;   /* byte offset of the GEMM_RS_DEBUG_TRACE stamps in the workspace */
 } gemm_rs_info;

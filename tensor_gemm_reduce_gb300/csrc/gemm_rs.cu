@@ -49,7 +49,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->grid < 0 || d->band_m < 0) return GEMM_RS_ERR_INVALID_ARG;
   if (d->unit_rows != 0 && d->unit_rows != 8 && d->unit_rows != 16 && d->unit_rows != 32)
     return GEMM_RS_ERR_INVALID_ARG;
-  if (d->mma_ctas < 0 || d->mma_ctas > 2) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->mma_ctas < 0 || d->mma_ctas == 3 || d->mma_ctas > 4) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   // TMA coordinates and kernel indices are 32-bit.
@@ -108,15 +108,22 @@ long long items_of(long long blocks, int blocks_per_region, long long tail_regio
   return (blocks - tail_blocks) * splits + tail_blocks * (kBM / 4);
 }
 
-const void* gemm_kernel(bool fused, int pair) {
-  if (pair == 2)
+// ctas: CTAs of the cluster that share a tile (1, 2 or 4).
+const void* gemm_kernel(bool fused, int ctas) {
+  if (ctas == 4)
+    return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 4>)
+                 : reinterpret_cast<const void*>(gemm_rs_kernel<false, 4>);
+  if (ctas == 2)
     return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 2>)
                  : reinterpret_cast<const void*>(gemm_rs_kernel<false, 2>);
   return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 1>)
                : reinterpret_cast<const void*>(gemm_rs_kernel<false, 1>);
 }
 
-int gemm_smem(int pair) { return pair == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc; }
+int gemm_smem(int ctas) {
+  return ctas == 4 ? TileCfg<4>::kSmemAlloc
+                   : ctas == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc;
+}
 
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, bool fused,
                  int grid, int threads, cudaStream_t st) {
@@ -129,9 +136,9 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, b
   // by whichever CTAs run, and producers never wait for reducers.
   (void)fused;
   int n = 0;
-  if (pair == 2) {
+  if (pair > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.x = (unsigned)pair;
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -157,7 +164,7 @@ int launch_gemm_kernel(int pair, bool fused, int grid, int threads, const GemmPa
 // Set the shared-memory limit of the four GEMM kernels; persistent grid size
 // (CTAs) for `pair` CTAs per MMA: one CTA per SM, whole clusters only.
 int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_fused, int* grid) {
-  for (int pr = 1; pr <= 2; ++pr)
+  for (int pr = 1; pr <= 4; pr *= 2)
     for (int f = 0; f < 2; ++f)
       if (cudaFuncSetAttribute(gemm_kernel(f != 0, pr), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                gemm_smem(pr)) != cudaSuccess) {
@@ -166,20 +173,20 @@ int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_f
       }
   (void)dev;
   int g = requested > 0 && requested < num_sms ? requested : num_sms;
-  if (pair == 2) {
+  if (pair > 1) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    fill_launch(&cfg, attr, 2, false, 2 * (num_sms / 2), threads_fused, 0);
+    fill_launch(&cfg, attr, pair, false, pair * (num_sms / pair), threads_fused, 0);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel(true, 2), &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel(true, pair), &cfg) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_RS_ERR_CUDA;
     }
     if (clusters < 1) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
-    int pairs = g / 2;
-    if (pairs > clusters) pairs = clusters;
-    if (pairs < 1) pairs = 1;
-    g = 2 * pairs;
+    int n_clusters = g / pair;
+    if (n_clusters > clusters) n_clusters = clusters;
+    if (n_clusters < 1) n_clusters = 1;
+    g = pair * n_clusters;
   }
   *grid = g;
   return GEMM_RS_OK;

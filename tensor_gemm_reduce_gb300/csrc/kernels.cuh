@@ -44,11 +44,14 @@ constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
 constexpr int kMaxReducerWarps = 6;
 
-// Shared-memory plan of one CTA for 1 or 2 CTAs per MMA.
-template <int kPair>
+// Shared-memory plan of one CTA.  kCtas = CTAs of the cluster that share a
+// tile: 1 (one-CTA MMA), 2 (one 2-CTA MMA) or 4 (two 2-CTA MMAs on vertically
+// adjacent 256-row halves of the tile, sharing its W tile by TMA multicast).
+template <int kCtas>
 struct TileCfg {
-  static constexpr int kStages = kPair == 1 ? 4 : 6;
-  static constexpr int kTileRows = kBM * kPair;        // output rows of one (pair) tile
+  static constexpr int kPair = kCtas >= 2 ? 2 : 1;     // CTAs per MMA
+  static constexpr int kStages = kCtas == 1 ? 4 : 6;
+  static constexpr int kTileRows = kBM * kCtas;        // output rows of one cluster tile
   static constexpr int kBCols = kBN / kPair;           // W columns held by one CTA
   static constexpr int kBBoxes = kBCols / 64;          // 64-column TMA boxes per stage
   static constexpr int kBBoxBytes = kBK * 64 * 2;      // 8 KiB: 64 k-rows x 64 n, N-major
@@ -65,7 +68,6 @@ struct TileCfg {
   // tmem addr, abort, items reduced, pad, ring slots[4], tiles landed per epilogue warp[4]
   static constexpr int kSmemBytes = kSmemMisc + 16 + 4 * 4 + 4 * kEpiWarps;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack to align the base to 1024 bytes
-  static constexpr uint32_t kFlagAddsPerTile = kEpiWarps * kPair;
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 };
 
@@ -356,19 +358,20 @@ __device__ __forceinline__ void land_and_publish(const GemmParams& p, volatile u
 }
 
 // ---------------------------------------------------------------------------
-// Tile ring: the pair leader's TMA thread claims rank tiles from one atomic
-// ticket (so no tile waits for a CTA that is not running) and hands each tile
-// index to every consumer through a small ring in shared memory, mirrored
-// into the peer CTA.  Consumers: the MMA thread (leader), the 4 epilogue
-// warps of each CTA and, in a pair, the peer's TMA thread.  Index -1 ends the
-// stream.
-template <int kPair>
+// Tile ring: the cluster's first CTA claims tiles from one atomic ticket (so
+// no tile waits for a CTA that is not running) and hands each tile index to
+// every consumer through a small ring in shared memory, mirrored into the
+// other CTAs of the cluster.  Consumers: the MMA thread of each MMA leader,
+// the 4 epilogue warps of each CTA and the TMA thread of every other CTA.
+// Index -1 ends the stream.
+template <int kCtas>
 struct TileRing {
   static constexpr int kDepth = 4;
-  static constexpr uint32_t kConsumers = kPair == 1 ? 1 + kEpiWarps : 2 + 2 * kEpiWarps;
+  static constexpr uint32_t kConsumers =
+      kCtas == 1 ? 1 + kEpiWarps : kCtas == 2 ? 2 + 2 * kEpiWarps : 2 + 4 * kEpiWarps + 3;
   uint32_t slots;   // shared address of int32 slot[kDepth]
   uint32_t full;    // shared address of mbarrier full[kDepth]
-  uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in the leader)
+  uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in CTA 0)
   int slot = 0;
   uint32_t phase = 0;
 
@@ -378,23 +381,24 @@ struct TileRing {
       phase ^= 1u;
     }
   }
-  // Producer (leader TMA thread): publish the next claimed tile, or -1.
+  // Producer (CTA 0's TMA thread): publish the next claimed tile, or -1.
   __device__ __forceinline__ bool put(int tile, uint64_t limit, volatile uint32_t* abort) {
-    if (!bar_wait<kPair == 2>(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
+    if (!bar_wait<(kCtas > 1)>(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
     st_shared_u32(slots + 4 * slot, (uint32_t)tile);
     mbar_arrive(full + 8 * slot);
-    if constexpr (kPair == 2) {
-      st_shared_cluster_u32(mapa_shared(slots + 4 * slot, 1), (uint32_t)tile);
-      mbar_arrive_cluster(mapa_shared(full + 8 * slot, 1));
+#pragma unroll
+    for (uint32_t r = 1; r < (uint32_t)kCtas; ++r) {
+      st_shared_cluster_u32(mapa_shared(slots + 4 * slot, r), (uint32_t)tile);
+      mbar_arrive_cluster(mapa_shared(full + 8 * slot, r));
     }
     advance();
     return true;
   }
   // Consumer: next tile index (-1 at the end); false if the wait gave up.
   __device__ __forceinline__ bool get(int* tile, uint64_t limit, volatile uint32_t* abort) {
-    if (!bar_wait<kPair == 2>(full + 8 * slot, phase, limit, abort)) return false;
+    if (!bar_wait<(kCtas > 1)>(full + 8 * slot, phase, limit, abort)) return false;
     *tile = (int)ld_shared_u32(slots + 4 * slot);
-    if constexpr (kPair == 2)
+    if constexpr (kCtas > 1)
       mbar_arrive_cluster(mapa_shared(empty + 8 * slot, 0));
     else
       mbar_arrive(empty + 8 * slot);
@@ -404,20 +408,24 @@ struct TileRing {
 };
 
 // ---------------------------------------------------------------------------
-// The persistent GEMM kernel.  kFused = true adds flags and reducer warps;
-// kPair = 2 shares each MMA between the two CTAs of a cluster.
-template <bool kFused, int kPair>
+// The persistent GEMM kernel.  kFused = true adds completion publication and
+// reducer warps; kCtas selects the tile shape (see TileCfg).
+template <bool kFused, int kCtas>
 __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps : 0)), 1)
     gemm_rs_kernel(const __grid_constant__ GemmParams p) {
-  using C = TileCfg<kPair>;
-  using Ring = TileRing<kPair>;
+  using C = TileCfg<kCtas>;
+  using Ring = TileRing<kCtas>;
+  constexpr int kPair = C::kPair;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t cta_rank = kPair == 2 ? cluster_ctarank() : 0u;
-  const bool leader = cta_rank == 0;
+  const uint32_t cta_rank = kCtas > 1 ? cluster_ctarank() : 0u;
+  const bool first_cta = cta_rank == 0;                  // claims the cluster's tiles
+  const uint32_t half = cta_rank % kPair;                // which CTA of its MMA pair
+  const uint32_t mma_leader_rank = cta_rank - half;      // issues the pair's MMAs
+  const bool mma_leader = half == 0;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::kSmemBar;
   const uint32_t bar_empty = bar_full + 8 * C::kStages;
@@ -436,8 +444,11 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);   // the leader's expect-tx arrival (+ bytes of the pair)
-      mbar_init(bar_empty + 8 * s, 1);  // one MMA commit
+      // the MMA leader's expect-tx arrival (+ the bytes landing in its pair)
+      mbar_init(bar_full + 8 * s, 1);
+      // one MMA commit per MMA pair writing into this stage (4 CTAs: both pairs,
+      // since both pairs' W loads land in every CTA)
+      mbar_init(bar_empty + 8 * s, kCtas == 4 ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_acc_full + 8 * b, 1);
@@ -463,7 +474,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (kPair == 2) cluster_sync();  // the peer's barriers exist before any remote use
+  if constexpr (kCtas > 1) cluster_sync();  // every CTA's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   unsigned long long* trace =
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       while (true) {
         int idx = -1;
         bool ok;
-        if (leader) {  // claim the next tile for the pair and publish it
+        if (first_cta) {  // claim the next tile for the cluster and publish it
           const uint32_t t = atomicAdd(p.ctrl + kCtrlTileTicket * kCtrlStride, 1u);
           idx = (long long)t < p.num_tiles ? (int)t : -1;
           ok = ring.put(idx, limit, cta_abort);
@@ -496,9 +507,9 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
         if (idx < 0) break;
         const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
         const int m0 = tc.mt * C::kTileRows + (int)cta_rank * kBM;
-        const int n0 = tc.nt * kBN + (int)cta_rank * C::kBCols;
+        const int n0 = tc.nt * kBN + (int)half * C::kBCols;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!bar_wait(bar_empty + 8 * stage, phase ^ 1u, limit, cta_abort)) {
+          if (!bar_wait<kCtas == 4>(bar_empty + 8 * stage, phase ^ 1u, limit, cta_abort)) {
             if (!*cta_abort) {
               record_error(p, kErrPipeTimeout, kWhereTma, (uint32_t)idx);
               *cta_abort = 1;
@@ -509,21 +520,33 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sa = sbase + C::kSmemA + stage * C::kAStage;
           const uint32_t sb = sbase + C::kSmemB + stage * C::kBStage;
-          if constexpr (kPair == 1) {
+          if constexpr (kCtas == 1) {
             mbar_arrive_expect_tx(fb, C::kStage);
             tma_load_3d(sa, &p.tmap_a, fb, kb * kBK, m0, tc.rank);
 #pragma unroll
             for (int j = 0; j < C::kBBoxes; ++j)
               tma_load_3d(sb + j * C::kBBoxBytes, &p.tmap_b, fb, n0 + 64 * j, kb * kBK, tc.rank);
-          } else {
+          } else if constexpr (kCtas == 2) {
             // both CTAs' bytes are counted on the leader's barrier
-            if (leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
+            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
             const uint32_t fb_leader = mapa_shared(fb, 0);
             tma_load_3d_pair(sa, &p.tmap_a, fb_leader, kb * kBK, m0, tc.rank);
 #pragma unroll
             for (int j = 0; j < C::kBBoxes; ++j)
               tma_load_3d_pair(sb + j * C::kBBoxBytes, &p.tmap_b, fb_leader, n0 + 64 * j,
                                kb * kBK, tc.rank);
+          } else {
+            // each pair's leader counts the bytes landing in both CTAs of its
+            // pair: the CTAs' own A rows and the two 64-column W boxes of each
+            // CTA's column half, one loaded by each pair and multicast to the
+            // CTAs of both pairs that hold that half
+            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
+            const uint32_t fb_leader = mapa_shared(fb, mma_leader_rank);
+            tma_load_3d_pair(sa, &p.tmap_a, fb_leader, kb * kBK, m0, tc.rank);
+            const uint32_t pair_id = cta_rank >> 1;
+            const uint16_t mask = (uint16_t)((1u << half) | (1u << (half + 2)));
+            tma_load_3d_pair_multicast(sb + pair_id * C::kBBoxBytes, &p.tmap_b, fb_leader,
+                                       n0 + 64 * (int)pair_id, kb * kBK, tc.rank, mask);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -534,18 +557,18 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
         }
         if (!ok) break;
       }
-      // Let every copy this thread started land before the CTA can exit (the
-      // leader's barriers also count the peer's bytes).
-      if (leader)
+      // Let every copy this CTA started (or expects) land before it can exit
+      // (with a 2-CTA MMA the leader's barriers also count the peer's bytes).
+      if (kCtas == 1 || mma_leader)
         for (int s = 0; s < C::kStages; ++s)
           if (issued_mask & (1u << s))
             bar_wait(bar_full + 8 * s, (issued_par >> s) & 1u, limit, cta_abort);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_bf16_f32(C::kTileRows, kBN, /*b_mn_major=*/1);
+    if (lane == 0 && mma_leader) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * kPair, kBN, /*b_mn_major=*/1);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -559,7 +582,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
           break;
         }
         if (idx < 0) break;
-        if (!bar_wait<kPair == 2>(bar_acc_empty + 8 * acc, acc_phase ^ 1u, limit, cta_abort)) {
+        if (!bar_wait<(kCtas > 1)>(bar_acc_empty + 8 * acc, acc_phase ^ 1u, limit, cta_abort)) {
           if (!*cta_abort) {
             record_error(p, kErrPipeTimeout, kWhereMma, (uint32_t)idx);
             *cta_abort = 1;
@@ -590,22 +613,22 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             const uint64_t bd = smem_desc_sw128(sb + s * 2048, C::kBBoxBytes, 1024);
             mma_bf16<kPair>(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
           }
-          // frees the smem stage (in both CTAs) when these MMAs finish
-          if constexpr (kPair == 1)
+          // frees the smem stage (in every CTA a W load wrote into) when these MMAs finish
+          if constexpr (kCtas == 1)
             mma_commit<1>(bar_empty + 8 * stage);
           else
-            mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
+            mma_commit_pair_multicast(bar_empty + 8 * stage, kCtas == 4 ? 0xF : 0x3);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        // accumulator ready for the epilogue warps (of both CTAs)
-        if constexpr (kPair == 1)
+        // accumulator ready for the epilogue warps (of both CTAs of the pair)
+        if constexpr (kCtas == 1)
           mma_commit<1>(bar_acc_full + 8 * acc);
         else
-          mma_commit_pair_multicast(bar_acc_full + 8 * acc, 0x3);
+          mma_commit_pair_multicast(bar_acc_full + 8 * acc, (uint16_t)(0x3u << mma_leader_rank));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -668,7 +691,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             if constexpr (kPair == 1)
               mbar_arrive(bar_acc_empty + 8 * acc);
             else
-              mbar_arrive_cluster(mapa_shared(bar_acc_empty + 8 * acc, 0));
+              mbar_arrive_cluster(mapa_shared(bar_acc_empty + 8 * acc, mma_leader_rank));
           }
         }
         const int col0 = tc.nt * kBN + c * 64;
@@ -712,7 +735,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             land_and_publish(p, landed, ew, pend_n, pend_block, pend_skip, limit, cta_abort);
           }
           pend_block = ((int)(tc.mt * p.nt_count + tc.nt)) * p.blocks_per_region + (int)cta_rank;
-          pend_skip = (p.debug_flags & 1u) && idx == 0 && leader;
+          pend_skip = (p.debug_flags & 1u) && idx == 0 && first_cta;
         }
         __syncwarp();
       }
@@ -738,7 +761,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   if (trace && lane == 0) atomicMax(trace + 3, (unsigned long long)globaltimer_ns());
   tc_fence_before();
   __syncthreads();
-  if constexpr (kPair == 2) cluster_sync();  // no MMA or remote arrive targets this CTA any more
+  if constexpr (kCtas > 1) cluster_sync();  // no MMA or remote arrive targets this CTA any more
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<kPair>(tmem_base, kTmemCols);

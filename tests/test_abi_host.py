@@ -40,6 +40,7 @@ def _create(**kw):
     (dict(unit_rows=64), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(grid=-2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(mma_ctas=3), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(mma_ctas=5), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(N=12), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(K=96), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
@@ -67,7 +68,7 @@ def test_strerror(lib):
     assert G.strerror(-99) == "unknown status"
 
 
-@pytest.mark.parametrize("ctas", [1, 2])
+@pytest.mark.parametrize("ctas", [1, 2, 4])
 @pytest.mark.parametrize("M,N,K,band", [(128, 512, 1024, 0), (392, 776, 1600, 0),
                                         (2048, 8192, 8192, 0), (8192, 8192, 28672, 0),
                                         (1000, 6144, 6144, 3), (520, 1000, 1024, 1)])
@@ -100,7 +101,7 @@ def test_schedule_band_walks_columns_inside_band(lib):
     assert regions[16] == (4, 0)
 
 
-@pytest.mark.parametrize("ctas", [1, 2])
+@pytest.mark.parametrize("ctas", [1, 2, 4])
 def test_auto_band_keeps_a_rows_within_budget(lib, ctas):
     rows = 128 * ctas
     for M, K in [(2048, 8192), (8192, 28672), (32768, 16384), (512, 6144)]:

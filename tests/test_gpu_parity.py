@@ -40,7 +40,7 @@ def _full_check(A_bits, W_bits, check_partials=True, **kw):
     return c, fv, out
 
 
-@pytest.mark.parametrize("ctas", [1, 2])
+@pytest.mark.parametrize("ctas", [1, 2, 4])
 def test_tiny_workload(ctas):
     A, W = workloads.make_inputs(workloads.TINY)
     _full_check(A, W, mma_ctas=ctas)
@@ -57,6 +57,7 @@ def test_ragged_and_small_shapes(M, N, K):
     A, W = workloads.make_shape_inputs(M, N, K, seed=M + N + K)
     _full_check(A, W)
     _full_check(A, W, mma_ctas=1)
+    _full_check(A, W, mma_ctas=4)
 
 
 @pytest.mark.parametrize("kw", [dict(reducer_warps=1), dict(reducer_warps=6), dict(grid=3),
@@ -65,7 +66,8 @@ def test_ragged_and_small_shapes(M, N, K):
                                 dict(debug_flags=G.DEBUG_NO_STAGING_L2),
                                 dict(mma_ctas=1), dict(mma_ctas=1, unit_rows=32, grid=5),
                                 dict(mma_ctas=1, unit_rows=8, reducer_warps=1),
-                                dict(mma_ctas=2, band_m=1, unit_rows=32)])
+                                dict(mma_ctas=2, band_m=1, unit_rows=32),
+                                dict(mma_ctas=4), dict(mma_ctas=4, grid=8, reducer_warps=2)])
 def test_plan_variants(kw):
     A, W = workloads.make_shape_inputs(520, 1000, 1024, seed=9)
     _full_check(A, W, **kw)
