@@ -56,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--overlap-iters", type=int, default=200)
+    p.add_argument("--chunks", type=lambda s: [int(x) for x in s.split(",") if x], default=[2, 4, 8],
+                   help="chunk counts of the stream-overlap comparison (empty: skip it)")
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -284,18 +286,22 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("fused and unfused outputs differ")
 
     # overlap efficiency: per-iteration medians of each kernel alone
-    def time_mode(mode, iters, warm):
+    def time_mode(mode, iters, warm, pl=None, w=None):
+        pl = plan if pl is None else pl
+        w = ws if w is None else w
         for _ in range(warm):
-            plan.run(A, W, out, ws, mode)
+            pl.run(A, W, out, w, mode)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(iters)]
         torch.cuda.synchronize()
         for s, e in ev:
             s.record(stream)
-            plan.run(A, W, out, ws, mode)
+            pl.run(A, W, out, w, mode)
             e.record(stream)
         torch.cuda.synchronize()
-        check()
+        rc = pl.status()
+        if rc != G.GEMM_RS_OK:
+            raise RuntimeError(f"device status: {G.strerror(rc)}")
         return metrics.median(s.elapsed_time(e) for s, e in ev) * 1e-3
 
     it = args.overlap_iters
@@ -304,6 +310,23 @@ def run_ours(args, rank, world, local):
     t_fused = time_mode(G.FUSED, it, 20)
     t_unfused = time_mode(G.UNFUSED, it, 20)
     eff = metrics.overlap_efficiency(t_gemm, t_rs, t_fused)
+
+    # the prior stream-overlap method (row chunks, reduce of chunk c beside the
+    # GEMM of chunk c+1 on a second stream), on a workspace of its own
+    ws_c = None
+    t_chunked = {}
+    for c in args.chunks:
+        cplan = G.Plan(M, N, K, chunks=c)
+        if ws_c is None:
+            ws_c = cplan.new_workspace()
+        cplan.run(A, W, out, ws_c, G.CHUNKED)
+        torch.cuda.synchronize()
+        if not torch.equal(f0.view(torch.int16), out.view(torch.int16)):
+            raise RuntimeError(f"chunked ({c}) and fused outputs differ")
+        t_chunked[str(cplan.info.chunks)] = time_mode(G.CHUNKED, it, 10, cplan, ws_c)
+        cplan.close()
+    del ws_c
+    t_chunked_best = min(t_chunked.values()) if t_chunked else None
 
     # the contract's timed region: K fused steps between events
     for _ in range(args.warmup):
@@ -383,6 +406,9 @@ def run_ours(args, rank, world, local):
         "overlap": {"efficiency": eff, "t_gemm_us": t_gemm * 1e6, "t_rs_us": t_rs * 1e6,
                     "t_fused_us": t_fused * 1e6, "t_unfused_us": t_unfused * 1e6,
                     "fused_speedup_vs_unfused": t_unfused / t_fused, "iters": it,
+                    "t_chunked_us": {c: t * 1e6 for c, t in t_chunked.items()},
+                    "fused_speedup_vs_best_chunked":
+                        (t_chunked_best / t_fused) if t_chunked_best else None,
                     "statistic": "median of per-iteration CUDA-event times, rank 0"},
         "roofline": roof,
         "rs_roofline": rs_roof,

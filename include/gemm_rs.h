@@ -55,7 +55,11 @@ enum gemm_rs_mode {
   GEMM_RS_FUSED = 0,     /* one persistent kernel: tile GEMM + flagged reduce-scatter */
   GEMM_RS_UNFUSED = 1,   /* GEMM kernel writes the staging, then a separate reduce kernel */
   GEMM_RS_GEMM_ONLY = 2, /* only the GEMM kernel (per-rank partials into staging) */
-  GEMM_RS_RS_ONLY = 3    /* only the reduce kernel (reads the staging as it is) */
+  GEMM_RS_RS_ONLY = 3,   /* only the reduce kernel (reads the staging as it is) */
+  GEMM_RS_CHUNKED = 4    /* the prior stream-overlap method: the rows are cut into chunks;
+                            the GEMM of chunk c runs on `stream` while the reduce kernel
+                            of chunk c-1 runs on a second stream of the plan (FLUX page,
+                            Figures 3 and 5); a comparison baseline, same result bits */
 };
 
 /* Debug switches (gemm_rs_desc.debug_flags). */
@@ -92,6 +96,8 @@ typedef struct gemm_rs_desc {
   int32_t mma_ctas;       /* CTAs of a cluster sharing one tile: 1 (128 x 256 tiles), 2 (a
                              2-CTA MMA, 256 x 256 tiles) or 4 (two 2-CTA MMAs, 512 x 256
                              tiles, W tiles shared by TMA multicast); 0 = 2 */
+  int32_t chunks;         /* CHUNKED: row chunks, 1..64; 0 = 4 (each a whole number of tile
+                             rows, the last one ragged) */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -110,10 +116,11 @@ typedef struct gemm_rs_info {
   int64_t units;          /* reduce items per FUSED run */
   int64_t workspace_bytes;
   int64_t staging_bytes;  /* 8 * M * N * 2 */
-  int32_t launches[4];    /* kernels launched per gemm_rs_run, indexed by mode */
+  int32_t launches[5];    /* kernels launched per gemm_rs_run, indexed by mode */
   int32_t mma_ctas;       /* CTAs of a cluster sharing one tile */
   int32_t tile_rows;      /* output rows of one rank tile: 128 * mma_ctas */
   int64_t trace_offset;   /* byte offset of the GEMM_RS_DEBUG_TRACE stamps in the workspace */
+  int32_t chunks;         /* CHUNKED: chunks actually used */
 } gemm_rs_info;
 
 /*
@@ -137,7 +144,9 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
  * partials of that GEMM; after FUSED it holds no defined values (reduced
  * staging lines are dropped from L2 without write-back when N % 64 == 0).
  * Returns after enqueueing; device-side failures (timeouts) are reported by
- * gemm_rs_status.  Modes that do not read A/W (RS_ONLY) or write out
+ * gemm_rs_status.  CHUNKED also uses a second stream and events that the plan
+ * creates on its first CHUNKED call; that stream joins `stream` again before
+ * the call returns (work after it on `stream` sees the whole output).  Modes that do not read A/W (RS_ONLY) or write out
  * (GEMM_ONLY) accept NULL for them.
  */
 int gemm_rs_run(gemm_rs_t plan, int mode, const void* A, const void* W,

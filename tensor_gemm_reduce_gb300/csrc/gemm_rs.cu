@@ -21,6 +21,8 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultReducerWarps = 4;
 constexpr int kDefaultUnitRows = 16;
 constexpr int kDefaultMmaCtas = 2;
+constexpr int kDefaultChunks = 4;
+constexpr int kMaxChunks = 64;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -50,6 +52,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->unit_rows != 0 && d->unit_rows != 8 && d->unit_rows != 16 && d->unit_rows != 32)
     return GEMM_RS_ERR_INVALID_ARG;
   if (d->mma_ctas < 0 || d->mma_ctas == 3 || d->mma_ctas > 4) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->chunks < 0 || d->chunks > kMaxChunks) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   // TMA coordinates and kernel indices are 32-bit.
@@ -210,6 +213,11 @@ struct gemm_rs_plan_s {
   void* map_ws = nullptr;
   bool maps_valid = false;
   GemmParams params;
+  // CHUNKED: row chunks, and the second stream and events (created on first use)
+  int chunks = 0, chunk_rows = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_chunk[kMaxChunks] = {};
 };
 
 extern "C" {
@@ -298,6 +306,14 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   h->tail_region = tail_region_of(h->tiles, h->grid / pair, (long long)h->mt * h->nt);
   h->items = items_of(blocks, h->blocks_per_region, h->tail_region, h->splits);
   h->lay = layout_for(d->M, d->N, blocks, h->items);
+  {  // CHUNKED: whole tile rows per chunk
+    const int want = d->chunks > 0 ? d->chunks : kDefaultChunks;
+    const long long per = (d->M + want - 1) / want;
+    long long rows = (per + h->tile_rows - 1) / h->tile_rows * h->tile_rows;
+    if (rows < 8) rows = 8;
+    h->chunk_rows = (int)rows;
+    h->chunks = d->M > 0 ? (int)((d->M + rows - 1) / rows) : 0;
+  }
   if (h->d.timeout_ns == 0) h->d.timeout_ns = kDefaultTimeoutNs;
   if (workspace_bytes) *workspace_bytes = h->lay.total;
   *plan = h;
@@ -325,6 +341,8 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->launches[GEMM_RS_UNFUSED] = empty ? 0 : (h->d.K == 0 ? 1 : 2);
   info->launches[GEMM_RS_GEMM_ONLY] = empty ? 0 : 1;
   info->launches[GEMM_RS_RS_ONLY] = empty ? 0 : 1;
+  info->launches[GEMM_RS_CHUNKED] = empty ? 0 : (h->d.K == 0 ? 1 : 2 * h->chunks);
+  info->chunks = h->chunks;
   info->mma_ctas = h->pair;
   info->tile_rows = h->tile_rows;
   info->trace_offset = (int64_t)h->lay.trace_off;
@@ -332,6 +350,14 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
 }
 
 int gemm_rs_destroy(gemm_rs_t h) {
+  if (!h) return GEMM_RS_OK;
+  if (h->side) {
+    cudaStreamDestroy(h->side);
+    cudaEventDestroy(h->ev_fork);
+    cudaEventDestroy(h->ev_join);
+    for (int c = 0; c < kMaxChunks; ++c)
+      if (h->ev_chunk[c]) cudaEventDestroy(h->ev_chunk[c]);
+  }
   delete h;
   return GEMM_RS_OK;
 }
@@ -341,16 +367,78 @@ static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
                             32 * (kGemmWarps + (fused ? h->reducer_warps : 0)), h->params, st);
 }
 
-static int launch_rs(gemm_rs_t h, const void* ws, void* out, cudaStream_t st) {
-  const long long mn = (long long)h->d.M * h->d.N;
-  long long nvec = mn / 8;
-  long long blocks = (nvec + 255) / 256;
+// Reduce kernel over output rows [row0, row0 + rows).
+static int launch_rs_rows(gemm_rs_t h, const void* ws, void* out, long long row0, long long rows,
+                          cudaStream_t st) {
+  const long long plane = (long long)h->d.M * h->d.N;
+  const long long elems = rows * h->d.N;
+  long long blocks = (elems / 8 + 255) / 256;
   const long long cap = (long long)h->num_sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  rs_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(ws),
-                                                     static_cast<uint16_t*>(out), mn);
+  rs_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+      static_cast<const uint16_t*>(ws) + row0 * h->d.N,
+      static_cast<uint16_t*>(out) + row0 * h->d.N, elems, plane);
   return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
+}
+
+static int launch_rs(gemm_rs_t h, const void* ws, void* out, cudaStream_t st) {
+  return launch_rs_rows(h, ws, out, 0, h->d.M, st);
+}
+
+// The prior stream-overlap method: GEMM of chunk c on `st`, reduce of chunk c
+// on the plan's second stream once that GEMM is done, so the reduce of chunk c
+// overlaps the GEMM of chunk c+1.  Same kernels and arithmetic as UNFUSED.
+static int run_chunked(gemm_rs_t h, const void* A, void* out, void* ws, cudaStream_t st) {
+  if (!h->side) {
+    if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_RS_ERR_CUDA;
+    }
+    for (int c = 0; c < h->chunks; ++c)
+      if (cudaEventCreateWithFlags(&h->ev_chunk[c], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_RS_ERR_CUDA;
+      }
+  }
+  const gemm_rs_desc& d = h->d;
+  const uint64_t Kr = (uint64_t)(d.K / kWorld);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  if (cudaEventRecord(h->ev_fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(h->side, h->ev_fork, 0) != cudaSuccess)
+    return GEMM_RS_ERR_CUDA;
+  for (int c = 0; c < h->chunks; ++c) {
+    const long long row0 = (long long)c * h->chunk_rows;
+    long long rows = d.M - row0;
+    if (rows > h->chunk_rows) rows = h->chunk_rows;
+    GemmParams p = h->params;  // the whole problem's maps and settings, narrowed to the chunk
+    if (!make_map(&p.tmap_a, static_cast<const uint8_t*>(A) + row0 * Kr * 2, Kr, (uint64_t)rows,
+                  kWorld, Kr * 2, Kr * 2 * (uint64_t)d.M, kBK, kBM) ||
+        !make_map(&p.tmap_st, wsb + row0 * d.N * 2, (uint64_t)d.N, (uint64_t)rows, kWorld,
+                  (uint64_t)d.N * 2, (uint64_t)d.N * 2 * (uint64_t)d.M, 64, 32))
+      return GEMM_RS_ERR_CUDA;
+    p.M = (int)rows;
+    p.mt_count = (int)((rows + h->tile_rows - 1) / h->tile_rows);
+    p.num_tiles = (long long)kWorld * p.mt_count * h->nt;
+    p.band = d.band_m > 0 ? (d.band_m < p.mt_count ? d.band_m : p.mt_count)
+                          : auto_band(rows, d.K, h->tile_rows);
+    if (p.band < 1) p.band = 1;
+    p.staging_in_l2 = 0;
+    p.trace = nullptr;
+    int rc = launch_gemm_kernel(h->pair, false, h->grid, 32 * kGemmWarps, p, st);
+    if (rc != GEMM_RS_OK) return rc;
+    if (cudaEventRecord(h->ev_chunk[c], st) != cudaSuccess ||
+        cudaStreamWaitEvent(h->side, h->ev_chunk[c], 0) != cudaSuccess)
+      return GEMM_RS_ERR_CUDA;
+    rc = launch_rs_rows(h, wsb, out, row0, rows, h->side);
+    if (rc != GEMM_RS_OK) return rc;
+  }
+  if (cudaEventRecord(h->ev_join, h->side) != cudaSuccess ||
+      cudaStreamWaitEvent(st, h->ev_join, 0) != cudaSuccess)
+    return GEMM_RS_ERR_CUDA;
+  return GEMM_RS_OK;
 }
 
 static int launch_zero(gemm_rs_t h, void* p, size_t bytes, cudaStream_t st) {
@@ -366,7 +454,7 @@ static int launch_zero(gemm_rs_t h, void* p, size_t bytes, cudaStream_t st) {
 int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, void* ws,
                 void* stream) {
   if (!h) return GEMM_RS_ERR_INVALID_ARG;
-  if (mode < GEMM_RS_FUSED || mode > GEMM_RS_RS_ONLY) return GEMM_RS_ERR_INVALID_ARG;
+  if (mode < GEMM_RS_FUSED || mode > GEMM_RS_CHUNKED) return GEMM_RS_ERR_INVALID_ARG;
   const gemm_rs_desc& d = h->d;
   if (d.M == 0 || d.N == 0) return GEMM_RS_OK;  // nothing to read or write
   // A and W hold no element when K == 0: their pointers are not used then.
@@ -464,6 +552,9 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     case GEMM_RS_RS_ONLY:
       rc = launch_rs(h, wsb, out, st);
       break;
+    case GEMM_RS_CHUNKED:
+      rc = run_chunked(h, h->map_A, out, wsb, st);
+      break;
   }
   if (rc != GEMM_RS_OK) cudaGetLastError();
   return rc;
@@ -505,7 +596,7 @@ extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const
                                 void* out_host, void* A_dev, void* W_dev, void* out_dev,
                                 void* ws, void* stream) {
   if (!h) return GEMM_RS_ERR_INVALID_ARG;
-  if (mode < GEMM_RS_FUSED || mode > GEMM_RS_RS_ONLY) return GEMM_RS_ERR_INVALID_ARG;
+  if (mode < GEMM_RS_FUSED || mode > GEMM_RS_CHUNKED) return GEMM_RS_ERR_INVALID_ARG;
   const bool needs_ab = mode != GEMM_RS_RS_ONLY;
   const bool needs_out = mode != GEMM_RS_GEMM_ONLY;
   const gemm_rs_desc& d = h->d;

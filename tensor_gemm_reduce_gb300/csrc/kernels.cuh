@@ -785,12 +785,14 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
 }
 
 // ---------------------------------------------------------------------------
-// Standalone reduce-scatter kernel of the unfused path: the same arithmetic
-// (reduce8) over the whole output, one 16-byte vector per thread and step.
+// Standalone reduce-scatter kernel of the unfused and chunked paths: the same
+// arithmetic (reduce8) over `elems` consecutive output elements, one 16-byte
+// vector per thread and step.  stage points at rank 0's first element; rank
+// r's partial of the same element is `plane` elements further per rank.
 __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restrict__ stage,
                                                         uint16_t* __restrict__ out,
-                                                        long long mn) {
-  const long long nvec = mn / 8;
+                                                        long long elems, long long plane) {
+  const long long nvec = elems / 8;
   const long long stride = (long long)gridDim.x * blockDim.x;
   long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
 #pragma unroll 1
@@ -798,8 +800,8 @@ __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restri
     uint4 a[kWorld], b[kWorld];
 #pragma unroll
     for (int r = 0; r < kWorld; ++r) {
-      a[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * mn) + v);
-      b[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * mn) + v + stride);
+      a[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * plane) + v);
+      b[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * plane) + v + stride);
     }
     reinterpret_cast<uint4*>(out)[v] = reduce8(a);
     reinterpret_cast<uint4*>(out)[v + stride] = reduce8(b);
@@ -808,7 +810,7 @@ __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restri
     uint4 a[kWorld];
 #pragma unroll
     for (int r = 0; r < kWorld; ++r)
-      a[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * mn) + v);
+      a[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * plane) + v);
     reinterpret_cast<uint4*>(out)[v] = reduce8(a);
   }
 }

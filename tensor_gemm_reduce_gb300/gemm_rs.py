@@ -36,8 +36,9 @@ GEMM_RS_ERR_INCOMPLETE = -9
 # Fixed scratch of the no-allocation entry point (see gemm_rs_fused_noalloc).
 NOALLOC_STAGING_BYTES = 32 << 20
 
-FUSED, UNFUSED, GEMM_ONLY, RS_ONLY = 0, 1, 2, 3
-MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": RS_ONLY}
+FUSED, UNFUSED, GEMM_ONLY, RS_ONLY, CHUNKED = 0, 1, 2, 3, 4
+MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": RS_ONLY,
+         "chunked": CHUNKED}
 
 DEBUG_SKIP_ONE_FLAG = 0x1
 DEBUG_NO_STAGING_L2 = 0x2
@@ -57,6 +58,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("timeout_ns", ctypes.c_uint64),
         ("debug_flags", ctypes.c_uint32),
         ("mma_ctas", ctypes.c_int32),
+        ("chunks", ctypes.c_int32),
     ]
 
 
@@ -75,10 +77,11 @@ class gemm_rs_info(ctypes.Structure):
         ("units", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
         ("staging_bytes", ctypes.c_int64),
-        ("launches", ctypes.c_int32 * 4),
+        ("launches", ctypes.c_int32 * 5),
         ("mma_ctas", ctypes.c_int32),
         ("tile_rows", ctypes.c_int32),
         ("trace_offset", ctypes.c_int64),
+        ("chunks", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -155,9 +158,9 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          mma_ctas=0, world=WORLD):
+          mma_ctas=0, chunks=0, world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas)
+                        debug_flags, mma_ctas, chunks)
 
 
 # ----------------------------------------------------------------------------
@@ -235,10 +238,10 @@ class Plan:
 
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
-                 mma_ctas: int = 0):
+                 mma_ctas: int = 0, chunks: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
-                          timeout_ns, debug_flags, mma_ctas)
+                          timeout_ns, debug_flags, mma_ctas, chunks)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property

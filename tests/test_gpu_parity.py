@@ -75,6 +75,54 @@ def test_plan_variants(kw):
     _full_check(A, W, **kw)
 
 
+@pytest.mark.parametrize("M,N,K,kw", [
+    (1024, 1280, 2048, dict(chunks=4)),              # 4 chunks of 256 rows
+    (1024, 1280, 2048, dict(chunks=3)),              # 3 chunks: 512, 512 and none -> 2 used
+    (392, 776, 1600, dict(chunks=2)),                # ragged M, N, K; last chunk 136 rows
+    (392, 776, 1600, dict(chunks=8, mma_ctas=1)),    # 128-row tiles: chunks of 128, 128, 128, 8
+    (2048, 512, 1024, dict(chunks=8, mma_ctas=4)),   # 512-row tiles: 4 chunks
+    (8, 256, 512, dict(chunks=4)),                   # one chunk of 8 rows
+    (520, 1000, 1024, dict(chunks=1, band_m=1)),     # a single chunk is the unfused path
+])
+def test_chunked_matches_unfused_bitwise(M, N, K, kw):
+    """The stream-overlap comparison mode: the same GEMM tiles and the same
+    reduce arithmetic, only cut into row chunks on two streams."""
+    A, W = workloads.make_shape_inputs(M, N, K, seed=M + 3 * N + K)
+    c = Case(A, W, **kw)
+    info = c.plan.info
+    per = -(-M // kw["chunks"])
+    rows = max(8, -(-per // info.tile_rows) * info.tile_rows)
+    assert info.chunks == -(-M // rows)
+    assert info.launches[G.CHUNKED] == 2 * info.chunks
+    unf = c.run(G.UNFUSED, poison=True)
+    for _ in range(2):
+        ch = c.run(G.CHUNKED, poison=True)
+        assert torch.equal(ch.view(torch.int16), unf.view(torch.int16))
+    out, _ = oracle.gemm_rs(A, W)
+    assert_parity(to_host_values(ch), out, None)
+    # the fused kernel on the same workspace afterwards is still clean
+    assert torch.equal(c.run(G.FUSED, poison=True).view(torch.int16), unf.view(torch.int16))
+
+
+def test_chunked_zero_k_and_host_copies():
+    p = G.Plan(64, 128, 0, chunks=2)
+    ws = p.new_workspace()
+    out = torch.full((64, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    p.run(torch.empty(8, 64, 0, dtype=torch.bfloat16, device="cuda"),
+          torch.empty(8, 0, 128, dtype=torch.bfloat16, device="cuda"), out, ws, G.CHUNKED)
+    assert p.status() == G.GEMM_RS_OK
+    assert torch.count_nonzero(out).item() == 0
+    A, W = workloads.make_shape_inputs(264, 1536, 2048, seed=31)
+    c = Case(A, W, chunks=4)
+    ref = c.run(G.UNFUSED)
+    A_h = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_h = torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_h = torch.empty(264, 1536, dtype=torch.bfloat16).pin_memory()
+    c.plan.run_host(A_h, W_h, out_h, c.A, c.W, c.out, c.ws, G.CHUNKED)
+    assert c.plan.status() == G.GEMM_RS_OK
+    assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16).cpu())
+
+
 def test_exact_integer_case():
     g = np.random.Generator(np.random.PCG64(3))
     M, N, K = 136, 264, 1024
