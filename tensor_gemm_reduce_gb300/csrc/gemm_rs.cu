@@ -415,10 +415,9 @@ static int run_chunked(gemm_rs_t h, const void* A, void* out, void* ws, cudaStre
     if (rows > h->chunk_rows) rows = h->chunk_rows;
     GemmParams p = h->params;  // the whole problem's maps and settings, narrowed to the chunk
     if (!make_map(&p.tmap_a, static_cast<const uint8_t*>(A) + row0 * Kr * 2, Kr, (uint64_t)rows,
-                  kWorld, Kr * 2, Kr * 2 * (uint64_t)d.M, kBK, kBM) ||
-        !make_map(&p.tmap_st, wsb + row0 * d.N * 2, (uint64_t)d.N, (uint64_t)rows, kWorld,
-                  (uint64_t)d.N * 2, (uint64_t)d.N * 2 * (uint64_t)d.M, 64, 32))
+                  kWorld, Kr * 2, Kr * 2 * (uint64_t)d.M, kBK, kBM))
       return GEMM_RS_ERR_CUDA;
+    p.stage = reinterpret_cast<uint16_t*>(wsb) + row0 * d.N;  // rank planes stay M * N apart
     p.M = (int)rows;
     p.mt_count = (int)((rows + h->tile_rows - 1) / h->tile_rows);
     p.num_tiles = (long long)kWorld * p.mt_count * h->nt;
@@ -498,10 +497,8 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
                     (uint64_t)d.N * 2 * Kr, 64, kBK))
         return GEMM_RS_ERR_CUDA;
     }
-    if (!make_map(&p.tmap_st, wsb, (uint64_t)d.N, (uint64_t)d.M, kWorld, (uint64_t)d.N * 2,
-                  (uint64_t)d.N * 2 * (uint64_t)d.M, 64, 32))
-      return GEMM_RS_ERR_CUDA;
-    p.stage = reinterpret_cast<const uint16_t*>(wsb);
+    p.stage = reinterpret_cast<uint16_t*>(wsb);
+    p.plane = d.M * d.N;
     p.flags = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
     p.queue = reinterpret_cast<unsigned long long*>(wsb + h->lay.queue_off);
     p.ctrl = reinterpret_cast<uint32_t*>(wsb + h->lay.ctrl_off);
@@ -537,7 +534,8 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
       h->params.staging_in_l2 = (d.N % 64 == 0) && !(d.debug_flags & GEMM_RS_DEBUG_NO_STAGING_L2);
       h->epoch += 1;
       h->params.epoch = h->epoch;
-      h->params.flag_target = (uint32_t)kWorld * h->epoch;  // every rank adds 1 per block
+      // every epilogue warp of every rank adds 1 per block and run
+      h->params.flag_target = (uint32_t)(kWorld * kEpiWarps) * h->epoch;
       rc = launch_gemm(h, true, st);
       break;
     case GEMM_RS_UNFUSED:
@@ -735,11 +733,10 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     const uint64_t Kr = (uint64_t)(K / kWorld);
     if (!make_map(&p.tmap_a, A, Kr, (uint64_t)M, kWorld, Kr * 2, Kr * 2 * (uint64_t)M, kBK, kBM) ||
         !make_map(&p.tmap_b, W, (uint64_t)N, Kr, kWorld, (uint64_t)N * 2, (uint64_t)N * 2 * Kr, 64,
-                  kBK) ||
-        !make_map(&p.tmap_st, scratch, (uint64_t)N, (uint64_t)M, kWorld, (uint64_t)N * 2,
-                  (uint64_t)N * 2 * (uint64_t)M, 64, 32))
+                  kBK))
       return GEMM_RS_ERR_CUDA;
-    p.stage = reinterpret_cast<const uint16_t*>(scratch);
+    p.stage = reinterpret_cast<uint16_t*>(scratch);
+    p.plane = M * N;
     p.out = static_cast<uint16_t*>(out);
     p.flags = flags;
     p.queue = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(flags) +
@@ -761,7 +758,7 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     const long long tail = tail_region_of(p.num_tiles, nd->grid / kDefaultMmaCtas, mt * nt);
     p.tail_region = (int)tail;
     p.num_items = items_of(blocks, p.blocks_per_region, tail, p.splits);
-    p.flag_target = (uint32_t)kWorld;  // counts were just cleared: one run's worth of adds
+    p.flag_target = (uint32_t)(kWorld * kEpiWarps);  // counts were just cleared: one run's adds
     p.timeout_ns = kDefaultTimeoutNs;
     rc = launch_gemm_kernel(kDefaultMmaCtas, true, nd->grid,
                             32 * (kGemmWarps + kDefaultReducerWarps), p, st);

@@ -19,13 +19,14 @@
 //   warp 1        MMA issuer (the pair's first CTA only): tcgen05.mma
 //                 (bf16 in, fp32 in TMEM, two 256-column accumulators);
 //                 TMEM allocation in every CTA
-//   warps 2..5    epilogue: TMEM -> registers -> bf16 (RNE) -> swizzled smem ->
-//                 TMA store into the rank's staging region; then (fused kernel)
-//                 once the 4 warps' stores of the CTA's 128 rows of a tile
-//                 have landed, one thread publishes them with a release add on
-//                 that 128-row block's completion count; the rank tile that
-//                 completes a block (the 8th add) appends the block's reduce
-//                 items to a global FIFO
+//   warps 2..5    epilogue: TMEM -> registers -> bf16 (RNE) -> an 8 x 8
+//                 transpose of 16-byte granules inside each 8-lane group ->
+//                 coalesced stores into the rank's staging region (every store
+//                 instruction writes four whole 128-byte row segments); then
+//                 (fused kernel) each warp publishes its 32 rows with a release
+//                 add on the 128-row block's completion count; the add that
+//                 completes a block (the last of 8 ranks x 4 warps) appends the
+//                 block's reduce items to a global FIFO
 //   warps 6..     reducers (fused kernel only): take the next FIFO position,
 //                 wait (acquire) until its item is there, add the 8 bf16
 //                 partials in fp32 in rank order, write bf16 output.  The
@@ -39,7 +40,6 @@
 namespace grs {
 
 constexpr int kEpiWarps = 4;
-constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16 columns
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
 constexpr int kMaxReducerWarps = 6;
@@ -47,10 +47,12 @@ constexpr int kMaxReducerWarps = 6;
 // Shared-memory plan of one CTA.  kCtas = CTAs of the cluster that share a
 // tile: 1 (one-CTA MMA), 2 (one 2-CTA MMA) or 4 (two 2-CTA MMAs on vertically
 // adjacent 256-row halves of the tile, sharing its W tile by TMA multicast).
+// The epilogue needs no shared memory, so all of it but the barriers holds
+// operand stages: the loads are latency-bound, and each stage more hides more.
 template <int kCtas>
 struct TileCfg {
   static constexpr int kPair = kCtas >= 2 ? 2 : 1;     // CTAs per MMA
-  static constexpr int kStages = kCtas == 1 ? 4 : 6;
+  static constexpr int kStages = kCtas == 1 ? 4 : 7;
   static constexpr int kTileRows = kBM * kCtas;        // output rows of one cluster tile
   static constexpr int kBCols = kBN / kPair;           // W columns held by one CTA
   static constexpr int kBBoxes = kBCols / 64;          // 64-column TMA boxes per stage
@@ -60,13 +62,12 @@ struct TileCfg {
   static constexpr int kStage = kAStage + kBStage;     // bytes one CTA loads per stage
   static constexpr int kSmemA = 0;
   static constexpr int kSmemB = kSmemA + kStages * kAStage;
-  static constexpr int kSmemEpi = kSmemB + kStages * kBStage;
-  static constexpr int kSmemBar = kSmemEpi + kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kSmemBar = kSmemB + kStages * kBStage;
   // full[S], empty[S], acc_full[2], acc_empty[2], drain, tile ring full[4], empty[4]
   static constexpr int kNumBars = 2 * kStages + 5 + 2 * 4;
   static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
-  // tmem addr, abort, items reduced, pad, ring slots[4], tiles landed per epilogue warp[4]
-  static constexpr int kSmemBytes = kSmemMisc + 16 + 4 * 4 + 4 * kEpiWarps;
+  // tmem addr, abort, items reduced, pad, ring slots[4]
+  static constexpr int kSmemBytes = kSmemMisc + 16 + 4 * 4;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack to align the base to 1024 bytes
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 };
@@ -96,13 +97,13 @@ enum ErrWhere : uint32_t { kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereRe
 struct GemmParams {
   CUtensorMap tmap_a;   // A  [8][M][Kr] : dims {Kr, M, 8}, box {64, 128, 1}
   CUtensorMap tmap_b;   // W  [8][Kr][N] : dims {N, Kr, 8}, box {64, 64, 1}
-  CUtensorMap tmap_st;  // staging [8][M][N] : dims {N, M, 8}, box {64, 32, 1}
-  const uint16_t* stage;
+  uint16_t* stage;   // rank r's partial of output element (i, j): stage[r * plane + i * N + j]
+  long long plane;   // elements from one rank's staging region to the next
   uint16_t* out;
   // Completion count per 128-row block of the output (a region's blocks are
-  // consecutive, one per CTA of the pair): every rank's tile adds 1 per fused
-  // run, so a run's target is 8 * (runs so far) and the add that reaches it
-  // completes the block.
+  // consecutive, one per CTA of the pair): each of the 4 epilogue warps of
+  // every rank's tile adds 1 per fused run, so a run's target is
+  // 32 * (runs so far) and the add that reaches it completes the block.
   uint32_t* flags;
   uint32_t* ctrl;   // kCtrlWords words (kCtrlCount words, kCtrlStride apart)
   int M, N, Kr;
@@ -263,7 +264,7 @@ __device__ __forceinline__ void reduce_rows(const GemmParams& p, size_t plane, i
 // [8l, 8l+8) of the block's 256).  With p.staging_in_l2 the staging lines
 // just read are dropped from L2.
 __device__ __forceinline__ void reduce_item(const GemmParams& p, int item, int lane) {
-  const size_t plane = (size_t)p.M * p.N;
+  const size_t plane = (size_t)p.plane;
   const int block = item >> 5;
   const int part = item & 31;
   const int region = block / p.blocks_per_region;
@@ -306,55 +307,44 @@ __device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_
   }
 }
 
-// Wait until at most n bulk groups of this thread are incomplete.
-__device__ __forceinline__ void bulk_wait_upto(int n) {
-  switch (n) {
-    case 0: bulk_wait_all<0>(); break;
-    case 1: bulk_wait_all<1>(); break;
-    case 2: bulk_wait_all<2>(); break;
-    case 3: bulk_wait_all<3>(); break;
-    default: bulk_wait_all<4>(); break;
-  }
-}
-
-// One rank's 128-row block of a tile is in global memory (all 4 epilogue
-// warps' stores landed and were fenced, then met on an smem barrier): count
-// it with a release add and, if it is the 8th rank, acquire the others and
-// queue the block's items.
-__device__ __forceinline__ void publish_block(const GemmParams& p, int block, bool skip) {
+// One epilogue warp's 32 rows of a rank tile are stored (and ordered before
+// this thread by __syncwarp): count them with a release add on the 128-row
+// block's completion count; the add that completes the block acquires the
+// other adds and queues the block's items.
+__device__ __forceinline__ void publish_rows(const GemmParams& p, int block, bool skip) {
   if (skip) return;  // debug: this completion never arrives
   const uint32_t old = atom_add_release_gpu(p.flags + (size_t)block * kFlagStride, 1u);
   if (old == p.flag_target - 1u) {
-    fence_acq_rel_gpu();  // acquire the other ranks' releases, release to the FIFO
+    fence_acq_rel_gpu();  // acquire the other warps' releases, release to the FIFO
     const int region = block / p.blocks_per_region;
     queue_push_block(p, block, region >= p.tail_region ? kBM / 4 : p.splits);
   }
 }
 
-// Epilogue warp `ew` has its rows of the n-th published tile in global memory
-// (stores complete and proxy-fenced): record it; warp 0 then waits until all
-// 4 warps recorded tile n and publishes the CTA's 128-row block once.
-__device__ __forceinline__ void land_and_publish(const GemmParams& p, volatile uint32_t* landed,
-                                                 int ew, int n, int block, bool skip,
-                                                 uint64_t limit, volatile uint32_t* cta_abort) {
-  __threadfence_block();
-  landed[ew] = (uint32_t)n;
-  if (ew != 0) return;
-  const uint64_t t0 = globaltimer_ns();
-  for (int w = 1; w < kEpiWarps; ++w) {
-    while ((int)(landed[w] - (uint32_t)n) < 0) {
-      if (*cta_abort || globaltimer_ns() - t0 > limit) {
-        if (!*cta_abort) {
-          record_error(p, kErrPipeTimeout, kWhereEpi, (uint32_t)block);
-          *cta_abort = 1;
-        }
-        return;
+// Transpose 8 x 8 granules of 16 bytes across the 8 lanes of a group (t =
+// lane & 7): before, x[j] is granule j of the lane's own row; after, x[j] is
+// granule t of the group's row j.  Three butterfly steps; in step m a lane
+// swaps with lane t ^ m the half of its granules whose index differs from t in
+// bit m.
+__device__ __forceinline__ void transpose_granules(uint32_t (&x)[8][4], int t) {
+#pragma unroll
+  for (int s = 0; s < 3; ++s) {
+    const int m = 4 >> s;
+    const bool upper = (t & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j & m) continue;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t send = upper ? x[j][k] : x[j | m][k];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (upper)
+          x[j][k] = recv;
+        else
+          x[j | m][k] = recv;
       }
-      __nanosleep(32);
     }
   }
-  __threadfence_block();
-  publish_block(p, block, skip);
 }
 
 // ---------------------------------------------------------------------------
@@ -363,7 +353,9 @@ __device__ __forceinline__ void land_and_publish(const GemmParams& p, volatile u
 // every consumer through a small ring in shared memory, mirrored into the
 // other CTAs of the cluster.  Consumers: the MMA thread of each MMA leader,
 // the 4 epilogue warps of each CTA and the TMA thread of every other CTA.
-// Index -1 ends the stream.
+// Index -1 ends the stream.  The copies in the other CTAs are written with
+// st.async, which completes their full barrier's transaction bytes, and
+// every signal is a CTA-scope arrive: no thread waits on a cluster fence.
 template <int kCtas>
 struct TileRing {
   static constexpr int kDepth = 4;
@@ -372,6 +364,7 @@ struct TileRing {
   uint32_t slots;   // shared address of int32 slot[kDepth]
   uint32_t full;    // shared address of mbarrier full[kDepth]
   uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in CTA 0)
+  bool owner;       // this CTA is CTA 0, which claims the tiles
   int slot = 0;
   uint32_t phase = 0;
 
@@ -383,25 +376,26 @@ struct TileRing {
   }
   // Producer (CTA 0's TMA thread): publish the next claimed tile, or -1.
   __device__ __forceinline__ bool put(int tile, uint64_t limit, volatile uint32_t* abort) {
-    if (!bar_wait<(kCtas > 1)>(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
+    if (!bar_wait(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
     st_shared_u32(slots + 4 * slot, (uint32_t)tile);
     mbar_arrive(full + 8 * slot);
 #pragma unroll
     for (uint32_t r = 1; r < (uint32_t)kCtas; ++r) {
-      st_shared_cluster_u32(mapa_shared(slots + 4 * slot, r), (uint32_t)tile);
-      mbar_arrive_cluster(mapa_shared(full + 8 * slot, r));
+      const uint32_t remote_full = mapa_shared(full + 8 * slot, r);
+      mbar_arrive_expect_tx_remote(remote_full, 4);
+      st_async_u32(mapa_shared(slots + 4 * slot, r), (uint32_t)tile, remote_full);
     }
     advance();
     return true;
   }
   // Consumer: next tile index (-1 at the end); false if the wait gave up.
   __device__ __forceinline__ bool get(int* tile, uint64_t limit, volatile uint32_t* abort) {
-    if (!bar_wait<(kCtas > 1)>(full + 8 * slot, phase, limit, abort)) return false;
+    if (!bar_wait(full + 8 * slot, phase, limit, abort)) return false;
     *tile = (int)ld_shared_u32(slots + 4 * slot);
-    if constexpr (kCtas > 1)
-      mbar_arrive_cluster(mapa_shared(empty + 8 * slot, 0));
-    else
+    if (kCtas == 1 || owner)
       mbar_arrive(empty + 8 * slot);
+    else
+      mbar_arrive_remote(mapa_shared(empty + 8 * slot, 0));
     advance();
     return true;
   }
@@ -434,8 +428,6 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   const uint32_t bar_drain = bar_acc_empty + 16;
   const uint32_t bar_ring_full = bar_drain + 8;
   const uint32_t bar_ring_empty = bar_ring_full + 8 * Ring::kDepth;
-  // tiles whose stores have landed, per epilogue warp (monotonic counts)
-  volatile uint32_t* landed = reinterpret_cast<volatile uint32_t*>(smem + C::kSmemMisc + 32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
   volatile uint32_t* cta_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kSmemMisc + 4);
   uint32_t* cta_reduced = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc + 8);
@@ -459,14 +451,12 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       mbar_init(bar_ring_full + 8 * s, 1);
       mbar_init(bar_ring_empty + 8 * s, Ring::kConsumers);
     }
-    for (int w = 0; w < kEpiWarps; ++w) landed[w] = 0;
     *cta_abort = 0;
     *cta_reduced = 0;
     fence_mbar_init();
     fence_proxy_async_shared();
     tma_prefetch_desc(&p.tmap_a);
     tma_prefetch_desc(&p.tmap_b);
-    tma_prefetch_desc(&p.tmap_st);
   }
   if (warp == 1) {
     tmem_alloc<kPair>(smem_u32(tmem_slot), kTmemCols);
@@ -480,20 +470,25 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   unsigned long long* trace =
       (p.trace && blockIdx.x < kMaxTraceCtas) ? p.trace + blockIdx.x * kTraceWords : nullptr;
   if (trace && threadIdx.x == 0) trace[0] = globaltimer_ns();
-  Ring ring{ring_slots, bar_ring_full, bar_ring_empty};
+  Ring ring{ring_slots, bar_ring_full, bar_ring_empty, first_cta};
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, issued_par = 0;
+      // The cluster's tiles come from one atomic ticket.  The next ticket is
+      // taken as soon as a tile is published, so the atomic's round trip
+      // overlaps this tile's loads instead of stalling the next tile's.
+      uint32_t* const ticket = p.ctrl + kCtrlTileTicket * kCtrlStride;
+      uint32_t next = first_cta ? atomicAdd(ticket, 1u) : 0u;
       while (true) {
         int idx = -1;
         bool ok;
-        if (first_cta) {  // claim the next tile for the cluster and publish it
-          const uint32_t t = atomicAdd(p.ctrl + kCtrlTileTicket * kCtrlStride, 1u);
-          idx = (long long)t < p.num_tiles ? (int)t : -1;
+        if (first_cta) {  // publish the claimed tile to the cluster, claim the one after
+          idx = (long long)next < p.num_tiles ? (int)next : -1;
           ok = ring.put(idx, limit, cta_abort);
+          if (ok && idx >= 0) next = atomicAdd(ticket, 1u);
         } else {
           ok = ring.get(&idx, limit, cta_abort);
         }
@@ -582,7 +577,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
           break;
         }
         if (idx < 0) break;
-        if (!bar_wait<(kCtas > 1)>(bar_acc_empty + 8 * acc, acc_phase ^ 1u, limit, cta_abort)) {
+        if (!bar_wait(bar_acc_empty + 8 * acc, acc_phase ^ 1u, limit, cta_abort)) {
           if (!*cta_abort) {
             record_error(p, kErrPipeTimeout, kWhereMma, (uint32_t)idx);
             *cta_abort = 1;
@@ -640,17 +635,14 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
     __syncwarp();
   } else if (warp < kGemmWarps) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp can read
+    const int q = warp & 3;     // TMEM lane quadrant this warp can read
     const int ew = warp - 2;
-    const uint32_t buf_s = sbase + C::kSmemEpi + ew * 2 * kEpiBufBytes;
-    uint8_t* buf_p = smem + C::kSmemEpi + ew * 2 * kEpiBufBytes;
+    const int t8 = lane & 7;    // granule this lane stores after the transpose
+    const int grp = lane & 24;  // first row of the lane's 8-row group
     const bool hint = kFused && p.staging_in_l2;
     const uint64_t keep_policy = hint ? policy_evict_last() : 0;
-    int acc = 0, buf = 0;
+    int acc = 0;
     uint32_t acc_phase = 0;
-    int pend_block = -1;     // block of the previous tile, published one tile late
-    bool pend_skip = false;
-    int pend_n = 0;          // tiles published so far (landed-barrier phase)
     while (true) {
       int idx = -1, got = 0;
       if (lane == 0) {
@@ -671,9 +663,8 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       if (idx < 0) break;
       const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
       tc_fence_after();
-      const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32;
-      const bool rows_in = row0 < p.M;
-      int groups = 0;  // bulk groups this tile commits (lane 0)
+      const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32 + grp;
+      uint16_t* stage_r = p.stage + (size_t)tc.rank * (size_t)p.plane;
 #pragma unroll 1
       for (int c = 0; c < kBN / 64; ++c) {
         uint32_t v0[32], v1[32];
@@ -688,69 +679,49 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (kPair == 1)
+            if (kPair == 1 || mma_leader)
               mbar_arrive(bar_acc_empty + 8 * acc);
             else
-              mbar_arrive_cluster(mapa_shared(bar_acc_empty + 8 * acc, mma_leader_rank));
+              mbar_arrive_remote(mapa_shared(bar_acc_empty + 8 * acc, mma_leader_rank));
           }
         }
-        const int col0 = tc.nt * kBN + c * 64;
-        if (rows_in && col0 < p.N) {
-          if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer has read it
-          __syncwarp();
-          uint8_t* rowp = buf_p + buf * kEpiBufBytes + lane * 128;
+        // granule j = the 8 columns [8j, 8j + 8) of this chunk of the lane's row
+        uint32_t x[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            x[j][k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+        }
+        transpose_granules(x, t8);
+        const int col = tc.nt * kBN + c * 64 + 8 * t8;
+        if (col < p.N) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            w.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            w.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            w.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-            // 128-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ (t % 8)
-            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) = w;
+            if (row0 + j < p.M) {
+              uint16_t* dst = stage_r + (size_t)(row0 + j) * p.N + col;
+              const uint4 w = make_uint4(x[j][0], x[j][1], x[j][2], x[j][3]);
+              if (hint)
+                st_global_v4_hint(dst, w, keep_policy);
+              else
+                st_global_v4(dst, w);
+            }
           }
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            if (hint)
-              tma_store_3d_hint(&p.tmap_st, buf_s + buf * kEpiBufBytes, col0, row0, tc.rank,
-                                keep_policy);
-            else
-              tma_store_3d(&p.tmap_st, buf_s + buf * kEpiBufBytes, col0, row0, tc.rank);
-            bulk_commit();
-            ++groups;
-          }
-          buf ^= 1;
         }
       }
       if (kFused) {
-        // Publish the previous tile's block now that this tile's stores are
-        // issued: its stores have had this tile's TMEM work to complete.
+        __syncwarp();  // the warp's stores are ordered before lane 0's release
         if (lane == 0) {
-          if (pend_block >= 0) {
-            bulk_wait_upto(groups);      // at most this tile's groups still in flight
-            fence_proxy_async_global();  // order the async-proxy writes before the release
-            ++pend_n;
-            land_and_publish(p, landed, ew, pend_n, pend_block, pend_skip, limit, cta_abort);
-          }
-          pend_block = ((int)(tc.mt * p.nt_count + tc.nt)) * p.blocks_per_region + (int)cta_rank;
-          pend_skip = (p.debug_flags & 1u) && idx == 0 && first_cta;
+          const int block =
+              ((int)(tc.mt * p.nt_count + tc.nt)) * p.blocks_per_region + (int)cta_rank;
+          publish_rows(p, block, (p.debug_flags & 1u) && idx == 0 && first_cta && ew == 0);
         }
         __syncwarp();
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) {
-      bulk_wait_all<0>();
-      if (kFused && pend_block >= 0) {
-        fence_proxy_async_global();
-        ++pend_n;
-        land_and_publish(p, landed, ew, pend_n, pend_block, pend_skip, limit, cta_abort);
-      }
-    }
-    __syncwarp();
     if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
     if (kFused) reducer_loop(p, lane, cta_reduced);  // out of tiles: help with the reduction
   } else {

@@ -56,9 +56,26 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
-// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+// Arrive on an mbarrier given by its shared::cluster address (possibly in
+// another CTA of the cluster), with the default release at CTA scope.  A
+// cluster-scope release would also make the arriving thread wait for its
+// outstanding memory operations, which stalls producers and epilogue warps.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Remote arrive that also expects `bytes` more transaction bytes this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+// 4-byte store into another CTA's shared memory that completes 4 transaction
+// bytes of an mbarrier in that CTA once the value is there (no fence needed).
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v,
+                                             uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+                   cluster_addr),
+               "r"(v), "r"(cluster_bar)
                : "memory");
 }
 
@@ -189,6 +206,17 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, uint32
 }
 // Drop a 128-byte line from L2 without writing it back; its contents become
 // undefined.  For scratch data that is dead after its last read.
+// 16-byte global store; with an L2 cache policy (createpolicy) in the _hint form.
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v4_hint(void* p, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void discard_l2_line(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
