@@ -58,6 +58,8 @@ def parse_args(argv=None):
     p.add_argument("--overlap-iters", type=int, default=200)
     p.add_argument("--chunks", type=lambda s: [int(x) for x in s.split(",") if x], default=[2, 4, 8],
                    help="chunk counts of the stream-overlap comparison (empty: skip it)")
+    p.add_argument("--no-allreduce", dest="allreduce", action="store_false",
+                   help="skip the GEMM + all-reduce timing (8 output copies)")
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -286,17 +288,18 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("fused and unfused outputs differ")
 
     # overlap efficiency: per-iteration medians of each kernel alone
-    def time_mode(mode, iters, warm, pl=None, w=None):
+    def time_mode(mode, iters, warm, pl=None, w=None, o=None):
         pl = plan if pl is None else pl
         w = ws if w is None else w
+        o = out if o is None else o
         for _ in range(warm):
-            pl.run(A, W, out, w, mode)
+            pl.run(A, W, o, w, mode)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(iters)]
         torch.cuda.synchronize()
         for s, e in ev:
             s.record(stream)
-            pl.run(A, W, out, w, mode)
+            pl.run(A, W, o, w, mode)
             e.record(stream)
         torch.cuda.synchronize()
         rc = pl.status()
@@ -327,6 +330,21 @@ def run_ours(args, rank, world, local):
         cplan.close()
     del ws_c
     t_chunked_best = min(t_chunked.values()) if t_chunked else None
+
+    # GEMM + all-reduce: the same reduction written to all 8 ranks' copies
+    t_ar = {}
+    if args.allreduce:
+        aplan = G.Plan(M, N, K, replicas=8)
+        ws_a = aplan.new_workspace()
+        out_a = torch.empty(*aplan.out_shape, dtype=torch.bfloat16, device="cuda")
+        for mode, name in ((G.FUSED, "fused"), (G.UNFUSED, "unfused")):
+            aplan.run(A, W, out_a, ws_a, mode)
+            torch.cuda.synchronize()
+            if not all(torch.equal(out_a[r].view(torch.int16), f0.view(torch.int16)) for r in (0, 7)):
+                raise RuntimeError(f"all-reduce ({name}) copies differ from the reduce-scatter output")
+            t_ar[name] = time_mode(mode, it, 10, aplan, ws_a, out_a)
+        aplan.close()
+        del ws_a, out_a
 
     # the contract's timed region: K fused steps between events
     for _ in range(args.warmup):
@@ -411,6 +429,7 @@ def run_ours(args, rank, world, local):
                     "t_chunked_us": {c: t * 1e6 for c, t in t_chunked.items()},
                     "fused_speedup_vs_best_chunked":
                         (t_chunked_best / t_fused) if t_chunked_best else None,
+                    "allreduce_us": {k: v * 1e6 for k, v in t_ar.items()},
                     "statistic": "median of per-iteration CUDA-event times, rank 0"},
         "roofline": roof,
         "rs_roofline": rs_roof,

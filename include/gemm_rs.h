@@ -10,6 +10,12 @@
  * The partials are summed across the ranks (reduce) and rank s keeps rows
  * [s*M/8, (s+1)*M/8) of the sum (scatter).
  *
+ * All-reduce variant (desc.replicas = 8; mKernel page, sections 3.1, 4 and
+ * 5.2, GEMM+AllReduce: reduce within the node, then every rank holds the
+ * whole sum): the same reduction, and the reducer of each output unit writes
+ * the sum into all 8 ranks' copies of the output, i.e. the all-gather of the
+ * reduced slices is fused into the reduction.
+ *
  * On one GPU the 8 ranks are virtual.  Each rank's bf16 partial tiles are
  * written to a separate staging region in device memory (standing in for the
  * peer's receive buffer) and published with a per-tile completion flag.
@@ -98,6 +104,10 @@ typedef struct gemm_rs_desc {
                              tiles, W tiles shared by TMA multicast); 0 = 2 */
   int32_t chunks;         /* CHUNKED: row chunks, 1..64; 0 = 4 (each a whole number of tile
                              rows, the last one ragged) */
+  int32_t replicas;       /* copies of the reduced output: 0 or 1 = reduce-scatter, out is
+                             [M][N] (rank s's slice = rows [s*M/8, (s+1)*M/8)); 8 =
+                             all-reduce, out is [8][M][N] and copy r is virtual rank r's
+                             full sum (bitwise the reduce-scatter output) */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -121,6 +131,7 @@ typedef struct gemm_rs_info {
   int32_t tile_rows;      /* output rows of one rank tile: 128 * mma_ctas */
   int64_t trace_offset;   /* byte offset of the GEMM_RS_DEBUG_TRACE stamps in the workspace */
   int32_t chunks;         /* CHUNKED: chunks actually used */
+  int32_t replicas;       /* 1 (reduce-scatter) or 8 (all-reduce) */
 } gemm_rs_info;
 
 /*
@@ -136,7 +147,8 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
 
 /*
  * Enqueue one execution on `stream` (a cudaStream_t; NULL = legacy default).
- * A: [8][M][K/8] bf16, W: [8][K/8][N] bf16, out: [M][N] bf16, workspace:
+ * A: [8][M][K/8] bf16, W: [8][K/8][N] bf16, out: [M][N] bf16 ([8][M][N] with
+ * replicas = 8), workspace:
  * >= workspace_bytes, 256-byte aligned is best, 16-byte aligned is required.
  * The caller may pass an uninitialised workspace: the first call that sees a
  * new workspace pointer clears its control words (a small memset on the
@@ -157,7 +169,7 @@ int gemm_rs_run(gemm_rs_t plan, int mode, const void* A, const void* W,
  * host memory.  Enqueued on `stream`, in this order: copy A_host -> A_dev
  * (8*M*(K/8)*2 bytes) and W_host -> W_dev (8*(K/8)*N*2 bytes), run `mode`
  * exactly as gemm_rs_run would on the device buffers, copy out_dev -> out_host
- * (M*N*2 bytes).  All six buffers belong to the caller; host buffers should be
+ * (replicas*M*N*2 bytes).  All six buffers belong to the caller; host buffers should be
  * pinned (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous,
  * and must stay valid until the stream has passed the copies.  RS_ONLY copies
  * nothing in, GEMM_ONLY copies nothing out.  Same return codes as gemm_rs_run,

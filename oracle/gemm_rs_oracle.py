@@ -126,6 +126,19 @@ def gemm_rs_rows(A_shards, W_shards, rows):
     return gemm_rs(A, W_shards)
 
 
+def gemm_allreduce(A_shards, W_shards):
+    """GEMM + all-reduce of the same layer: every rank ends with the whole sum.
+
+    mKernel page, sections 3.1, 4 and 5.2 (GEMM+AllReduce: a reduction within
+    the node, after which every GPU holds the complete output).  The sum is the
+    same rank-order fp32 fold of the bf16 partials as the reduce-scatter's;
+    rank r's copy is all M rows of it.  Returns (out[8][M][N], ref[M][N]).
+    """
+    out, ref = gemm_rs(A_shards, W_shards)
+    world = np.asarray(A_shards).shape[0]
+    return np.stack([out.copy() for _ in range(world)]), ref
+
+
 def slices(out: np.ndarray, world: int = WORLD):
     """Split the reduced output into the per-rank row slices of the scatter."""
     M = out.shape[0]

@@ -53,6 +53,7 @@ int check_desc(const gemm_rs_desc* d) {
     return GEMM_RS_ERR_INVALID_ARG;
   if (d->mma_ctas < 0 || d->mma_ctas == 3 || d->mma_ctas > 4) return GEMM_RS_ERR_INVALID_ARG;
   if (d->chunks < 0 || d->chunks > kMaxChunks) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->replicas != 0 && d->replicas != 1 && d->replicas != kWorld) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   // TMA coordinates and kernel indices are 32-bit.
@@ -94,6 +95,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int mma_ctas_of(const gemm_rs_desc* d) { return d->mma_ctas > 0 ? d->mma_ctas : kDefaultMmaCtas; }
+int replicas_of(const gemm_rs_desc* d) { return d->replicas > 1 ? d->replicas : 1; }
 
 // First region completed by the last wave of tiles (tiles are claimed in
 // order, `lanes` at a time; a region's 8 rank tiles are consecutive).
@@ -343,6 +345,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->launches[GEMM_RS_RS_ONLY] = empty ? 0 : 1;
   info->launches[GEMM_RS_CHUNKED] = empty ? 0 : (h->d.K == 0 ? 1 : 2 * h->chunks);
   info->chunks = h->chunks;
+  info->replicas = replicas_of(&h->d);
   info->mma_ctas = h->pair;
   info->tile_rows = h->tile_rows;
   info->trace_offset = (int64_t)h->lay.trace_off;
@@ -370,7 +373,7 @@ static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
 // Reduce kernel over output rows [row0, row0 + rows).
 static int launch_rs_rows(gemm_rs_t h, const void* ws, void* out, long long row0, long long rows,
                           cudaStream_t st) {
-  const long long plane = (long long)h->d.M * h->d.N;
+  const long long plane = (long long)h->d.M * h->d.N;  // between rank planes and output copies
   const long long elems = rows * h->d.N;
   long long blocks = (elems / 8 + 255) / 256;
   const long long cap = (long long)h->num_sms * 8;
@@ -378,7 +381,7 @@ static int launch_rs_rows(gemm_rs_t h, const void* ws, void* out, long long row0
   if (blocks < 1) blocks = 1;
   rs_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       static_cast<const uint16_t*>(ws) + row0 * h->d.N,
-      static_cast<uint16_t*>(out) + row0 * h->d.N, elems, plane);
+      static_cast<uint16_t*>(out) + row0 * h->d.N, elems, plane, replicas_of(&h->d), plane);
   return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
 }
 
@@ -481,7 +484,7 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
   if (d.K == 0) {  // empty contraction: every partial and the sum are zero
     if (mode == GEMM_RS_GEMM_ONLY) return launch_zero(h, wsb, h->lay.staging_bytes, st);
     if (mode == GEMM_RS_RS_ONLY) return launch_rs(h, wsb, out, st);
-    return launch_zero(h, out, (size_t)d.M * d.N * 2, st);
+    return launch_zero(h, out, (size_t)replicas_of(&d) * d.M * d.N * 2, st);
   }
 
   if (!h->maps_valid || (needs_ab && (A != h->map_A || W != h->map_W)) || ws != h->map_ws) {
@@ -499,6 +502,8 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     }
     p.stage = reinterpret_cast<uint16_t*>(wsb);
     p.plane = d.M * d.N;
+    p.replicas = replicas_of(&d);
+    p.out_stride = d.M * d.N;
     p.flags = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
     p.queue = reinterpret_cast<unsigned long long*>(wsb + h->lay.queue_off);
     p.ctrl = reinterpret_cast<uint32_t*>(wsb + h->lay.ctrl_off);
@@ -600,7 +605,7 @@ extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const
   const gemm_rs_desc& d = h->d;
   const size_t a_bytes = (size_t)d.M * (size_t)d.K * 2;  // 8 shards of M x K/8
   const size_t w_bytes = (size_t)d.K * (size_t)d.N * 2;  // 8 shards of K/8 x N
-  const size_t o_bytes = (size_t)d.M * (size_t)d.N * 2;
+  const size_t o_bytes = (size_t)replicas_of(&d) * (size_t)d.M * (size_t)d.N * 2;
   if ((needs_ab && a_bytes && (!A_host || !A_dev)) || (needs_ab && w_bytes && (!W_host || !W_dev)) ||
       (needs_out && o_bytes && (!out_host || !out_dev)))
     return GEMM_RS_ERR_INVALID_ARG;
@@ -737,6 +742,8 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
       return GEMM_RS_ERR_CUDA;
     p.stage = reinterpret_cast<uint16_t*>(scratch);
     p.plane = M * N;
+    p.replicas = 1;
+    p.out_stride = M * N;
     p.out = static_cast<uint16_t*>(out);
     p.flags = flags;
     p.queue = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(flags) +

@@ -100,6 +100,8 @@ struct GemmParams {
   uint16_t* stage;   // rank r's partial of output element (i, j): stage[r * plane + i * N + j]
   long long plane;   // elements from one rank's staging region to the next
   uint16_t* out;
+  int replicas;          // copies of the output: 1 (reduce-scatter) or 8 (all-reduce)
+  long long out_stride;  // elements from one output copy to the next
   // Completion count per 128-row block of the output (a region's blocks are
   // consecutive, one per CTA of the pair): each of the 4 epilogue warps of
   // every rank's tile adds 1 per fused run, so a run's target is
@@ -245,8 +247,12 @@ __device__ __forceinline__ void reduce_rows(const GemmParams& p, size_t plane, i
       for (int r = 0; r < kWorld; ++r)
         v[i][r] = __ldcg(reinterpret_cast<const uint4*>(p.stage + r * plane + off + (size_t)i * p.N));
 #pragma unroll
-    for (int i = 0; i < R; ++i)
-      *reinterpret_cast<uint4*>(p.out + off + (size_t)i * p.N) = reduce8(v[i]);
+    for (int i = 0; i < R; ++i) {
+      const uint4 o = reduce8(v[i]);
+#pragma unroll 1
+      for (int c = 0; c < p.replicas; ++c)  // all-reduce: every rank's copy
+        *reinterpret_cast<uint4*>(p.out + (size_t)c * p.out_stride + off + (size_t)i * p.N) = o;
+    }
   }
   if (p.staging_in_l2) {
     __syncwarp();  // every lane has consumed its loads (its stores depend on them)
@@ -759,10 +765,19 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
 // Standalone reduce-scatter kernel of the unfused and chunked paths: the same
 // arithmetic (reduce8) over `elems` consecutive output elements, one 16-byte
 // vector per thread and step.  stage points at rank 0's first element; rank
-// r's partial of the same element is `plane` elements further per rank.
+// r's partial of the same element is `plane` elements further per rank.  The
+// sum goes to `replicas` copies of the output, `out_stride` elements apart
+// (8 for the all-reduce).
+__device__ __forceinline__ void store_replicas(uint16_t* out, long long v, uint4 o, int replicas,
+                                               long long out_stride) {
+#pragma unroll 1
+  for (int c = 0; c < replicas; ++c) reinterpret_cast<uint4*>(out + c * out_stride)[v] = o;
+}
+
 __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restrict__ stage,
                                                         uint16_t* __restrict__ out,
-                                                        long long elems, long long plane) {
+                                                        long long elems, long long plane,
+                                                        int replicas, long long out_stride) {
   const long long nvec = elems / 8;
   const long long stride = (long long)gridDim.x * blockDim.x;
   long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -774,17 +789,18 @@ __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restri
       a[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * plane) + v);
       b[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * plane) + v + stride);
     }
-    reinterpret_cast<uint4*>(out)[v] = reduce8(a);
-    reinterpret_cast<uint4*>(out)[v + stride] = reduce8(b);
+    store_replicas(out, v, reduce8(a), replicas, out_stride);
+    store_replicas(out, v + stride, reduce8(b), replicas, out_stride);
   }
   if (v < nvec) {
     uint4 a[kWorld];
 #pragma unroll
     for (int r = 0; r < kWorld; ++r)
       a[r] = __ldcg(reinterpret_cast<const uint4*>(stage + r * plane) + v);
-    reinterpret_cast<uint4*>(out)[v] = reduce8(a);
+    store_replicas(out, v, reduce8(a), replicas, out_stride);
   }
 }
+
 
 // Zero fill (empty contraction, K = 0): n16 16-byte vectors.
 __global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ p, long long n16) {

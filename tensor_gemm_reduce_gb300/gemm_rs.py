@@ -59,6 +59,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("debug_flags", ctypes.c_uint32),
         ("mma_ctas", ctypes.c_int32),
         ("chunks", ctypes.c_int32),
+        ("replicas", ctypes.c_int32),
     ]
 
 
@@ -82,6 +83,7 @@ class gemm_rs_info(ctypes.Structure):
         ("tile_rows", ctypes.c_int32),
         ("trace_offset", ctypes.c_int64),
         ("chunks", ctypes.c_int32),
+        ("replicas", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -158,9 +160,9 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          mma_ctas=0, chunks=0, world=WORLD):
+          mma_ctas=0, chunks=0, replicas=0, world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas, chunks)
+                        debug_flags, mma_ctas, chunks, replicas)
 
 
 # ----------------------------------------------------------------------------
@@ -238,11 +240,17 @@ class Plan:
 
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
-                 mma_ctas: int = 0, chunks: int = 0):
+                 mma_ctas: int = 0, chunks: int = 0, replicas: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
+        self.replicas = max(1, int(replicas))
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
-                          timeout_ns, debug_flags, mma_ctas, chunks)
+                          timeout_ns, debug_flags, mma_ctas, chunks, replicas)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
+
+    @property
+    def out_shape(self):
+        """[M][N] (reduce-scatter) or [8][M][N] (all-reduce: one copy per rank)."""
+        return (self.M, self.N) if self.replicas == 1 else (self.replicas, self.M, self.N)
 
     @property
     def info(self) -> gemm_rs_info:
@@ -270,7 +278,7 @@ class Plan:
         Kr = self.K // WORLD
         a = self._check(A, (WORLD, self.M, Kr), "A")
         w = self._check(W, (WORLD, Kr, self.N), "W")
-        o = self._check(out, (self.M, self.N), "out")
+        o = self._check(out, self.out_shape, "out")
         if workspace is None or workspace.numel() * workspace.element_size() < self.workspace_bytes:
             raise ValueError("workspace missing or too small")
         s = stream if stream is not None else torch.cuda.current_stream()
@@ -286,12 +294,12 @@ class Plan:
         Kr = self.K // WORLD
         for t, shape, name in ((A_host, (WORLD, self.M, Kr), "A_host"),
                                (W_host, (WORLD, Kr, self.N), "W_host"),
-                               (out_host, (self.M, self.N), "out_host")):
+                               (out_host, self.out_shape, "out_host")):
             if t.dtype != torch.bfloat16 or tuple(t.shape) != shape or t.is_cuda or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous host bf16 tensor of shape {shape}")
         a = self._check(A, (WORLD, self.M, Kr), "A")
         w = self._check(W, (WORLD, Kr, self.N), "W")
-        o = self._check(out, (self.M, self.N), "out")
+        o = self._check(out, self.out_shape, "out")
         if workspace is None or workspace.numel() * workspace.element_size() < self.workspace_bytes:
             raise ValueError("workspace missing or too small")
         s = stream if stream is not None else torch.cuda.current_stream()
@@ -327,7 +335,8 @@ class Plan:
 def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Plan] = None):
     """One call of the row-parallel linear layer with reduce-scatter.
 
-    Returns (out, plan, workspace); out[s*M/8:(s+1)*M/8] is rank s's slice.
+    Returns (out, plan, workspace); out[s*M/8:(s+1)*M/8] is rank s's slice
+    (a plan made with replicas=8 gives the all-reduce: out[r] is rank r's copy).
     """
     import torch
     R, M, Kr = A.shape
@@ -335,7 +344,7 @@ def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Pl
     if plan is None:
         plan = Plan(M, N, Kr * R)
     if out is None:
-        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+        out = torch.empty(*plan.out_shape, dtype=torch.bfloat16, device=A.device)
     if workspace is None:
         workspace = plan.new_workspace(A.device)
     plan.run(A, W, out, workspace, mode)

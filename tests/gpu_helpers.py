@@ -36,7 +36,7 @@ class Case:
         self.W = to_dev(W_bits)
         self.plan = G.Plan(self.M, self.N, self.K, **plan_kw)
         self.ws = self.plan.new_workspace()
-        self.out = torch.empty(self.M, self.N, dtype=torch.bfloat16, device="cuda")
+        self.out = torch.empty(*self.plan.out_shape, dtype=torch.bfloat16, device="cuda")
 
     def run(self, mode=G.FUSED, check_status=True, poison=False):
         if poison:

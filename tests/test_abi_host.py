@@ -43,6 +43,8 @@ def _create(**kw):
     (dict(mma_ctas=5), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(chunks=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(chunks=65), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(replicas=2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(replicas=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(N=12), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(K=96), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),

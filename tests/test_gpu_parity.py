@@ -123,6 +123,51 @@ def test_chunked_zero_k_and_host_copies():
     assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16).cpu())
 
 
+@pytest.mark.parametrize("M,N,K,kw", [
+    (392, 776, 1600, {}),                 # ragged M, N and K
+    (264, 1536, 2048, {}),                # N % 64 == 0: staging kept in L2 and dropped
+    (1024, 1280, 2048, dict(mma_ctas=1)),
+    (2048, 512, 1024, dict(mma_ctas=4, chunks=3)),
+    (8, 256, 512, {}),                    # one row per rank's slice
+])
+def test_allreduce_copies_equal_reduce_scatter(M, N, K, kw):
+    """All-reduce (replicas = 8): every rank's copy is the whole reduce-scatter
+    output, bit for bit, in every mode; and the oracle's all-reduce."""
+    A, W = workloads.make_shape_inputs(M, N, K, seed=5 * M + N + K)
+    rs = Case(A, W, **kw)
+    ref = rs.run(G.UNFUSED, poison=True)
+    ar = Case(A, W, replicas=8, **kw)
+    assert ar.plan.info.replicas == 8 and tuple(ar.out.shape) == (8, M, N)
+    for mode in (G.FUSED, G.UNFUSED, G.CHUNKED, G.FUSED):
+        out = ar.run(mode, poison=True)
+        for r in range(8):
+            assert torch.equal(out[r].view(torch.int16), ref.view(torch.int16)), (mode, r)
+    ar.run(G.GEMM_ONLY)
+    out = ar.run(G.RS_ONLY, poison=False)
+    assert torch.equal(out[5].view(torch.int16), ref.view(torch.int16))
+    out8, _ = oracle.gemm_allreduce(A, W)
+    assert_parity(to_host_values(out).reshape(8 * M, N), out8.reshape(8 * M, N), None)
+
+
+def test_allreduce_zero_k_and_host_copies():
+    p = G.Plan(64, 128, 0, replicas=8)
+    ws = p.new_workspace()
+    out = torch.full((8, 64, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    p.run(torch.empty(8, 64, 0, dtype=torch.bfloat16, device="cuda"),
+          torch.empty(8, 0, 128, dtype=torch.bfloat16, device="cuda"), out, ws, G.FUSED)
+    assert p.status() == G.GEMM_RS_OK
+    assert torch.count_nonzero(out).item() == 0
+    A, W = workloads.make_shape_inputs(256, 512, 1024, seed=33)
+    c = Case(A, W, replicas=8)
+    ref = c.run(G.UNFUSED)
+    A_h = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16).pin_memory()
+    W_h = torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_h = torch.empty(8, 256, 512, dtype=torch.bfloat16).pin_memory()
+    c.plan.run_host(A_h, W_h, out_h, c.A, c.W, c.out, c.ws, G.FUSED)
+    assert c.plan.status() == G.GEMM_RS_OK
+    assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16).cpu())
+
+
 def test_exact_integer_case():
     g = np.random.Generator(np.random.PCG64(3))
     M, N, K = 136, 264, 1024

@@ -347,3 +347,20 @@ def test_error_metrics():
     ref = out + 0.01
     assert oracle.rel_vs_ref(out, ref) == pytest.approx(0.01 / 4.01)
     assert oracle.err_vs_oracle(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(16, 8, 16, 41), (24, 16, 64, 42)])
+def test_allreduce_every_rank_holds_the_brute_force_sum(M, N, K, seed):
+    """All-reduce (mKernel page, sections 3.1, 4, 5.2): each of the 8 copies is
+    the exact rank-order sum of the rounded partials, all M rows of it."""
+    A_sh, W_sh = workloads.make_shape_inputs(M, N, K, seed)
+    out8, ref = oracle.gemm_allreduce(A_sh, W_sh)
+    exact = brute_force(A_sh, W_sh)
+    assert out8.shape == (8, M, N)
+    for r in range(8):
+        assert np.array_equal(out8[r], exact), r
+    # rank s's slice of the reduce-scatter is rows [s*M/8, (s+1)*M/8) of every copy
+    rs, _ = oracle.gemm_rs(A_sh, W_sh)
+    for s_, sl in enumerate(oracle.slices(rs)):
+        h = M // 8
+        assert np.array_equal(out8[(s_ + 3) % 8][s_ * h:(s_ + 1) * h], sl)
