@@ -58,6 +58,8 @@ def parse_args(argv=None):
     p.add_argument("--overlap-iters", type=int, default=200)
     p.add_argument("--chunks", type=lambda s: [int(x) for x in s.split(",") if x], default=[2, 4, 8],
                    help="chunk counts of the stream-overlap comparison (empty: skip it)")
+    p.add_argument("--ag-workload", default="llama3_70b_qkv_m2048",
+                   help="all-gather + GEMM workload timed beside the main one ('' to skip)")
     p.add_argument("--no-allreduce", dest="allreduce", action="store_false",
                    help="skip the GEMM + all-reduce timing (8 output copies)")
     p.add_argument("--e2e-steps", type=int, default=50)
@@ -288,18 +290,20 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("fused and unfused outputs differ")
 
     # overlap efficiency: per-iteration medians of each kernel alone
-    def time_mode(mode, iters, warm, pl=None, w=None, o=None):
+    def time_mode(mode, iters, warm, pl=None, w=None, o=None, a=None, b=None):
         pl = plan if pl is None else pl
         w = ws if w is None else w
         o = out if o is None else o
+        a = A if a is None else a
+        b = W if b is None else b
         for _ in range(warm):
-            pl.run(A, W, o, w, mode)
+            pl.run(a, b, o, w, mode)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(iters)]
         torch.cuda.synchronize()
         for s, e in ev:
             s.record(stream)
-            pl.run(A, W, o, w, mode)
+            pl.run(a, b, o, w, mode)
             e.record(stream)
         torch.cuda.synchronize()
         rc = pl.status()
@@ -330,6 +334,34 @@ def run_ours(args, rank, world, local):
         cplan.close()
     del ws_c
     t_chunked_best = min(t_chunked.values()) if t_chunked else None
+
+    # the column-parallel partner layer: all-gather + GEMM, fused and unfused
+    ag = None
+    if args.ag_workload:
+        wa = workloads.WORKLOADS[args.ag_workload]
+        Ab, Wb = workloads.make_inputs(wa)
+        A_ag = torch.from_numpy(Ab.view(np.int16)).cuda().view(torch.bfloat16)
+        W_ag = torch.from_numpy(Wb.view(np.int16)).cuda().view(torch.bfloat16)
+        gplan = G.Plan(wa.M, wa.N, wa.K, op=G.OP_AG)
+        ws_g = gplan.new_workspace()
+        out_g = torch.empty(*gplan.out_shape, dtype=torch.bfloat16, device="cuda")
+        gplan.run(A_ag, W_ag, out_g, ws_g, G.UNFUSED)
+        torch.cuda.synchronize()
+        ref_g = out_g.clone()
+        gplan.run(A_ag, W_ag, out_g, ws_g, G.FUSED)
+        torch.cuda.synchronize()
+        if gplan.status() != G.GEMM_RS_OK or not torch.equal(ref_g.view(torch.int16), out_g.view(torch.int16)):
+            raise RuntimeError("all-gather + GEMM: fused and unfused outputs differ")
+        tg = {name: time_mode(mode, it, 10, gplan, ws_g, out_g, A_ag, W_ag)
+              for mode, name in ((G.GEMM_ONLY, "gemm"), (G.RS_ONLY, "gather"),
+                                 (G.FUSED, "fused"), (G.UNFUSED, "unfused"))}
+        ag = {"workload": wa.name, "M": wa.M, "N": wa.N, "K": wa.K,
+              "tflops_fused": metrics.gemm_flops(wa.M, wa.N, wa.K) / tg["fused"] / 1e12,
+              "overlap_efficiency": metrics.overlap_efficiency(tg["gemm"], tg["gather"], tg["fused"]),
+              "fused_speedup_vs_unfused": tg["unfused"] / tg["fused"],
+              **{f"t_{k}_us": v * 1e6 for k, v in tg.items()}}
+        gplan.close()
+        del ws_g, out_g, A_ag, W_ag, ref_g
 
     # GEMM + all-reduce: the same reduction written to all 8 ranks' copies
     t_ar = {}
@@ -431,6 +463,7 @@ def run_ours(args, rank, world, local):
                         (t_chunked_best / t_fused) if t_chunked_best else None,
                     "allreduce_us": {k: v * 1e6 for k, v in t_ar.items()},
                     "statistic": "median of per-iteration CUDA-event times, rank 0"},
+        "allgather_gemm": ag,
         "roofline": roof,
         "rs_roofline": rs_roof,
         "cpu_baseline": cpu,

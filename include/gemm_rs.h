@@ -68,12 +68,36 @@ enum gemm_rs_mode {
                             Figures 3 and 5); a comparison baseline, same result bits */
 };
 
+/* The layer a plan computes (gemm_rs_desc.op).
+ *
+ * GEMM_RS_OP_RS: the row-parallel layer above (GEMM, then reduce-scatter or
+ *   all-reduce).
+ * GEMM_RS_OP_AG: the column-parallel partner layer, all-gather then GEMM
+ *   (FLUX page, abstract and Figure 1: all-gather fused into the GEMM's
+ *   prologue; mKernel page, sections 3.1 and 4: the local shard first, then
+ *   the other shards in the order they arrive).  Rank r holds the row shard
+ *   A_r = A[r*M/8 : (r+1)*M/8, :] and the column shard W_r = W[:, r*N/8 :
+ *   (r+1)*N/8]; it gathers all of A and computes C_r = A W_r (bf16, fp32
+ *   accumulation, one rounding).  Layouts: A [8][M/8][K], W [8][K][N/8],
+ *   out [8][M][N/8], all row-major bf16; N % 64 == 0.  The workspace holds
+ *   the 8 gather buffers [8][M][K] (rank r's copy of every shard) instead of
+ *   staging.  Modes: FUSED (copy warps gather while the tiles that need a
+ *   shard wait for its completion counts), UNFUSED (a gather kernel, then the
+ *   GEMM), GEMM_ONLY (the GEMM from the gather buffers as they are), RS_ONLY
+ *   (the gather kernel alone); CHUNKED and replicas = 8 are not defined.
+ */
+#define GEMM_RS_OP_RS 0
+#define GEMM_RS_OP_AG 1
+
 /* Debug switches (gemm_rs_desc.debug_flags). */
 #define GEMM_RS_DEBUG_SKIP_ONE_FLAG 0x1u /* FUSED: one producer warp never publishes its
                                             completion, so its block is never queued, the
                                             reducer waiting for it gives up after
                                             timeout_ns and the run reports
-                                            GEMM_RS_ERR_TIMEOUT; tests the bounded wait */
+                                            GEMM_RS_ERR_TIMEOUT; tests the bounded wait
+                                            (all-gather: the first copy item is never
+                                            published, so the tiles that need that shard
+                                            wait until timeout_ns) */
 #define GEMM_RS_DEBUG_NO_STAGING_L2 0x2u /* FUSED: store staging tiles without the L2
                                             evict-last hint and keep them after reduction
                                             (by default reduced staging lines are dropped
@@ -93,7 +117,8 @@ enum gemm_rs_mode {
 typedef struct gemm_rs_desc {
   int32_t world;          /* tensor-parallel degree; must be 8 */
   int64_t M, N, K;        /* M%8 == 0, N%8 == 0, K%64 == 0 (so K/8 is a multiple of 8); 0 allowed */
-  int32_t reducer_warps;  /* FUSED: reducer warps per CTA, 1..6; 0 = default (4) */
+  int32_t reducer_warps;  /* FUSED: reducer warps per CTA (all-gather: copy warps), 1..6;
+                             0 = default (4; all-gather 2) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
   int32_t unit_rows;      /* rows per reduce item in FUSED mode: 8, 16 or 32; 0 = 16 */
@@ -108,6 +133,7 @@ typedef struct gemm_rs_desc {
                              [M][N] (rank s's slice = rows [s*M/8, (s+1)*M/8)); 8 =
                              all-reduce, out is [8][M][N] and copy r is virtual rank r's
                              full sum (bitwise the reduce-scatter output) */
+  int32_t op;             /* GEMM_RS_OP_RS (0) or GEMM_RS_OP_AG (1) */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -132,6 +158,9 @@ typedef struct gemm_rs_info {
   int64_t trace_offset;   /* byte offset of the GEMM_RS_DEBUG_TRACE stamps in the workspace */
   int32_t chunks;         /* CHUNKED: chunks actually used */
   int32_t replicas;       /* 1 (reduce-scatter) or 8 (all-reduce) */
+  int32_t op;             /* GEMM_RS_OP_RS or GEMM_RS_OP_AG */
+  int32_t ag_direct;      /* AG: own shard read from the input, not copied */
+  int64_t copy_items;     /* AG: copy items of a fused run */
 } gemm_rs_info;
 
 /*

@@ -24,6 +24,13 @@ Readings of points the pages leave open (each one is listed in the design doc):
   * the "FP32 reference" of the correctness rule is taken in float64: the
     unrounded sum of the exact partials.
 
+The column-parallel partner layer, all-gather then GEMM (FLUX page, abstract
+and Figure 1; mKernel page, section 4), is here too (ag_gemm): rank r holds
+rows [r*M/8, (r+1)*M/8) of A and columns [r*N/8, (r+1)*N/8) of W, gathers all
+rows of A (in rank order, which puts A back together) and computes
+C_r = A W_r, rounded once to bf16 from its exact value (the GPU accumulates
+in FP32, so parity there is a tolerance).
+
 Pins that tie this module to something other than itself live in
 tests/test_oracle_pins.py (exact rational brute force, closed forms, invariants
 and library routines).
@@ -137,6 +144,26 @@ def gemm_allreduce(A_shards, W_shards):
     out, ref = gemm_rs(A_shards, W_shards)
     world = np.asarray(A_shards).shape[0]
     return np.stack([out.copy() for _ in range(world)]), ref
+
+
+def ag_gemm(A_shards, W_shards):
+    """All-gather + GEMM.  A_shards [8][M/8][K] (row shards), W_shards [8][K][N/8]
+    (column shards).  The gather stacks the row shards in rank order; rank r's
+    output is C_r = bf16(A W_r).  Returns (C[8][M][N/8], ref[8][M][N/8]), ref
+    unrounded (float64)."""
+    A = np.concatenate(list(_as_values(A_shards)), axis=0)
+    Wv = _as_values(W_shards)
+    ref = np.stack([A @ Wv[r] for r in range(Wv.shape[0])])
+    return bf16_round(ref), ref
+
+
+def ag_gemm_rows(A_shards, W_shards, rows):
+    """ag_gemm at the given rows of the gathered A only (row i of every C_r
+    depends only on row i of A).  Returns (C[8][len(rows)][N/8], ref)."""
+    A = np.concatenate(list(_as_values(A_shards)), axis=0)[np.asarray(rows, dtype=np.int64)]
+    Wv = _as_values(W_shards)
+    ref = np.stack([A @ Wv[r] for r in range(Wv.shape[0])])
+    return bf16_round(ref), ref
 
 
 def slices(out: np.ndarray, world: int = WORLD):

@@ -19,10 +19,12 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultReducerWarps = 4;
+constexpr int kDefaultCopyWarps = 2;
 constexpr int kDefaultUnitRows = 16;
 constexpr int kDefaultMmaCtas = 2;
 constexpr int kDefaultChunks = 4;
 constexpr int kMaxChunks = 64;
+constexpr long long kCopyChunk = 32768;  // elements per all-gather copy item (64 KiB)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -44,6 +46,20 @@ Layout layout_for(int64_t M, int64_t N, int64_t blocks, int64_t items) {
   return l;
 }
 
+// All-gather + GEMM workspace: the 8 gather buffers [8][M][K], the 64
+// per-(rank, shard) copy counts, the control words, the debug stamps.
+Layout layout_ag(int64_t M, int64_t K) {
+  Layout l;
+  l.staging_bytes = (size_t)kWorld * (size_t)M * (size_t)K * 2;
+  l.flags_off = align_up(l.staging_bytes, 256);
+  l.flags_bytes = (size_t)kWorld * kWorld * kFlagStride * 4;
+  l.queue_off = align_up(l.flags_off + l.flags_bytes, 256);
+  l.ctrl_off = l.queue_off;
+  l.trace_off = l.ctrl_off + (size_t)kCtrlWords * 4;
+  l.total = l.trace_off + (size_t)kMaxTraceCtas * kTraceWords * 8;
+  return l;
+}
+
 int check_desc(const gemm_rs_desc* d) {
   if (!d) return GEMM_RS_ERR_INVALID_ARG;
   if (d->world != GEMM_RS_WORLD) return GEMM_RS_ERR_INVALID_ARG;
@@ -54,12 +70,20 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->mma_ctas < 0 || d->mma_ctas == 3 || d->mma_ctas > 4) return GEMM_RS_ERR_INVALID_ARG;
   if (d->chunks < 0 || d->chunks > kMaxChunks) return GEMM_RS_ERR_INVALID_ARG;
   if (d->replicas != 0 && d->replicas != 1 && d->replicas != kWorld) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->op != GEMM_RS_OP_RS && d->op != GEMM_RS_OP_AG) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->op == GEMM_RS_OP_AG && d->replicas > 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   // TMA coordinates and kernel indices are 32-bit.
   if (d->M > (1ll << 30) || d->N > (1ll << 30) || d->K / 8 > (1ll << 30))
     return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
-  const int64_t mt = (d->M + kBM - 1) / kBM, nt = (d->N + kBN - 1) / kBN;
+  if (d->op == GEMM_RS_OP_AG) {
+    // out rows of N/8 elements must stay 16-byte aligned; K is every rank's
+    if (d->N % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+    if (d->K > (1ll << 30) || (d->M / 8) * d->K > (1ll << 40)) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  }
+  const int64_t cols = d->op == GEMM_RS_OP_AG ? d->N / kWorld : d->N;
+  const int64_t mt = (d->M + kBM - 1) / kBM, nt = (cols + kBN - 1) / kBN;
   if (mt * nt * kWorld >= (1ll << 31)) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   return GEMM_RS_OK;
 }
@@ -113,16 +137,18 @@ long long items_of(long long blocks, int blocks_per_region, long long tail_regio
   return (blocks - tail_blocks) * splits + tail_blocks * (kBM / 4);
 }
 
-// ctas: CTAs of the cluster that share a tile (1, 2 or 4).
-const void* gemm_kernel(bool fused, int ctas) {
-  if (ctas == 4)
-    return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 4>)
-                 : reinterpret_cast<const void*>(gemm_rs_kernel<false, 4>);
-  if (ctas == 2)
-    return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 2>)
-                 : reinterpret_cast<const void*>(gemm_rs_kernel<false, 2>);
-  return fused ? reinterpret_cast<const void*>(gemm_rs_kernel<true, 1>)
-               : reinterpret_cast<const void*>(gemm_rs_kernel<false, 1>);
+// kind: Kind (GEMM only, fused reduce-scatter, fused all-gather); ctas: CTAs
+// of the cluster that share a tile (1, 2 or 4).
+template <int kKind>
+const void* kernel_for(int ctas) {
+  if (ctas == 4) return reinterpret_cast<const void*>(gemm_rs_kernel<kKind, 4>);
+  if (ctas == 2) return reinterpret_cast<const void*>(gemm_rs_kernel<kKind, 2>);
+  return reinterpret_cast<const void*>(gemm_rs_kernel<kKind, 1>);
+}
+const void* gemm_kernel(int kind, int ctas) {
+  if (kind == kKindRS) return kernel_for<kKindRS>(ctas);
+  if (kind == kKindAG) return kernel_for<kKindAG>(ctas);
+  return kernel_for<kKindGemm>(ctas);
 }
 
 int gemm_smem(int ctas) {
@@ -130,7 +156,7 @@ int gemm_smem(int ctas) {
                    : ctas == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc;
 }
 
-void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, bool fused,
+void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, int kind,
                  int grid, int threads, cudaStream_t st) {
   memset(cfg, 0, sizeof(*cfg));
   cfg->gridDim = dim3((unsigned)grid);
@@ -139,7 +165,7 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, b
   cfg->stream = st;
   // No co-residency is needed: GEMM tiles are claimed from an atomic ticket
   // by whichever CTAs run, and producers never wait for reducers.
-  (void)fused;
+  (void)kind;
   int n = 0;
   if (pair > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
@@ -152,26 +178,26 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, b
   cfg->numAttrs = n;
 }
 
-// One launch of the persistent GEMM kernel (fused or GEMM only).
-int launch_gemm_kernel(int pair, bool fused, int grid, int threads, const GemmParams& p,
+// One launch of the persistent GEMM kernel of the given Kind.
+int launch_gemm_kernel(int pair, int kind, int grid, int threads, const GemmParams& p,
                        cudaStream_t st) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  fill_launch(&cfg, attr, pair, fused, grid, threads, st);
+  fill_launch(&cfg, attr, pair, kind, grid, threads, st);
   void* args[] = {const_cast<GemmParams*>(&p)};
-  if (cudaLaunchKernelExC(&cfg, gemm_kernel(fused, pair), args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&cfg, gemm_kernel(kind, pair), args) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_RS_ERR_CUDA;
   }
   return GEMM_RS_OK;
 }
 
-// Set the shared-memory limit of the four GEMM kernels; persistent grid size
+// Set the shared-memory limit of the GEMM kernels; persistent grid size
 // (CTAs) for `pair` CTAs per MMA: one CTA per SM, whole clusters only.
 int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_fused, int* grid) {
   for (int pr = 1; pr <= 4; pr *= 2)
-    for (int f = 0; f < 2; ++f)
-      if (cudaFuncSetAttribute(gemm_kernel(f != 0, pr), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    for (int kind = kKindGemm; kind <= kKindAG; ++kind)
+      if (cudaFuncSetAttribute(gemm_kernel(kind, pr), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                gemm_smem(pr)) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_RS_ERR_CUDA;
@@ -181,9 +207,9 @@ int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_f
   if (pair > 1) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    fill_launch(&cfg, attr, pair, false, pair * (num_sms / pair), threads_fused, 0);
+    fill_launch(&cfg, attr, pair, kKindRS, pair * (num_sms / pair), threads_fused, 0);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel(true, pair), &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel(kKindRS, pair), &cfg) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_RS_ERR_CUDA;
     }
@@ -220,6 +246,10 @@ struct gemm_rs_plan_s {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaEvent_t ev_chunk[kMaxChunks] = {};
+  // all-gather + GEMM (op == GEMM_RS_OP_AG)
+  bool ag = false;
+  int shard_rows = 0, ag_direct = 0, chunks_per_shard = 0, first_round = 0;
+  long long copy_items = 0;
 };
 
 extern "C" {
@@ -248,9 +278,20 @@ int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t*
   if (rc) return rc;
   if (!rank || !mt || !nt) return GEMM_RS_ERR_INVALID_ARG;
   const int tile_rows = kBM * mma_ctas_of(d);
-  const int mtc = (int)((d->M + tile_rows - 1) / tile_rows), ntc = (int)((d->N + kBN - 1) / kBN);
+  const bool ag = d->op == GEMM_RS_OP_AG;
+  const int64_t cols = ag ? d->N / kWorld : d->N;
+  const int mtc = (int)((d->M + tile_rows - 1) / tile_rows), ntc = (int)((cols + kBN - 1) / kBN);
   const long long tiles = (long long)kWorld * mtc * ntc;
   if (idx < 0 || idx >= tiles) return GEMM_RS_ERR_INVALID_ARG;
+  if (ag) {  // rank after rank, own shard first, in bands
+    const int band =
+        d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K, tile_rows);
+    const TileCoord t = ag_tile_at(idx, mtc, ntc, (int)(d->M / kWorld), tile_rows, band);
+    *rank = t.rank;
+    *mt = t.mt;
+    *nt = t.nt;
+    return GEMM_RS_OK;
+  }
   const int band =
       d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K, tile_rows);
   const TileCoord t = tile_at(idx, mtc, ntc, band);
@@ -279,7 +320,11 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   if (prop.major != 10 || prop.minor != 3) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
   const int pair = mma_ctas_of(d);
   if (prop.sharedMemPerBlockOptin < (size_t)gemm_smem(pair)) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
-  const int reducer_warps = d->reducer_warps > 0 ? d->reducer_warps : kDefaultReducerWarps;
+  // reducer warps (reduce-scatter) or copy warps (all-gather: 2 keep the
+  // copies ahead of the tiles with the least interference)
+  const int reducer_warps = d->reducer_warps > 0 ? d->reducer_warps
+                            : d->op == GEMM_RS_OP_AG ? kDefaultCopyWarps
+                                                     : kDefaultReducerWarps;
   int grid = 0;
   rc = prepare_kernels(dev, prop.multiProcessorCount, pair, d->grid,
                        32 * (kGemmWarps + reducer_warps), &grid);
@@ -316,6 +361,27 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
     h->chunk_rows = (int)rows;
     h->chunks = d->M > 0 ? (int)((d->M + rows - 1) / rows) : 0;
   }
+  if (d->op == GEMM_RS_OP_AG) {
+    h->ag = true;
+    const int64_t cols = d->N / kWorld;  // each rank's column shard of W
+    h->nt = (int)((cols + kBN - 1) / kBN);
+    h->num_kb = (int)((d->K + kBK - 1) / kBK);
+    h->tiles = (long long)kWorld * h->mt * h->nt;
+    // bands inside one rank's GEMM: A rows of that rank's gathered buffer
+    h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt)
+                            : auto_band(d->M, d->K, h->tile_rows);
+    if (h->band < 1) h->band = 1;
+    h->shard_rows = (int)(d->M / kWorld);
+    h->ag_direct = h->shard_rows > 0 && h->shard_rows % h->tile_rows == 0;
+    const long long shard_elems = (long long)h->shard_rows * d->K;
+    h->chunks_per_shard = (int)((shard_elems + kCopyChunk - 1) / kCopyChunk);
+    h->first_round = h->ag_direct;
+    h->copy_items = (long long)(kWorld - h->first_round) * kWorld * h->chunks_per_shard;
+    h->items = 0;
+    h->tail_region = 0;
+    h->chunks = 0;
+    h->lay = layout_ag(d->M, d->K);
+  }
   if (h->d.timeout_ns == 0) h->d.timeout_ns = kDefaultTimeoutNs;
   if (workspace_bytes) *workspace_bytes = h->lay.total;
   *plan = h;
@@ -346,6 +412,13 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->launches[GEMM_RS_CHUNKED] = empty ? 0 : (h->d.K == 0 ? 1 : 2 * h->chunks);
   info->chunks = h->chunks;
   info->replicas = replicas_of(&h->d);
+  info->op = h->d.op;
+  if (h->ag) {
+    info->launches[GEMM_RS_RS_ONLY] = empty || h->d.K == 0 ? 0 : 1;  // the gather kernel
+    info->launches[GEMM_RS_CHUNKED] = 0;                           // not defined
+    info->ag_direct = h->ag_direct;
+    info->copy_items = h->copy_items;
+  }
   info->mma_ctas = h->pair;
   info->tile_rows = h->tile_rows;
   info->trace_offset = (int64_t)h->lay.trace_off;
@@ -366,7 +439,7 @@ int gemm_rs_destroy(gemm_rs_t h) {
 }
 
 static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
-  return launch_gemm_kernel(h->pair, fused, h->grid,
+  return launch_gemm_kernel(h->pair, fused ? kKindRS : kKindGemm, h->grid,
                             32 * (kGemmWarps + (fused ? h->reducer_warps : 0)), h->params, st);
 }
 
@@ -429,7 +502,7 @@ static int run_chunked(gemm_rs_t h, const void* A, void* out, void* ws, cudaStre
     if (p.band < 1) p.band = 1;
     p.staging_in_l2 = 0;
     p.trace = nullptr;
-    int rc = launch_gemm_kernel(h->pair, false, h->grid, 32 * kGemmWarps, p, st);
+    int rc = launch_gemm_kernel(h->pair, kKindGemm, h->grid, 32 * kGemmWarps, p, st);
     if (rc != GEMM_RS_OK) return rc;
     if (cudaEventRecord(h->ev_chunk[c], st) != cudaSuccess ||
         cudaStreamWaitEvent(h->side, h->ev_chunk[c], 0) != cudaSuccess)
@@ -453,10 +526,115 @@ static int launch_zero(gemm_rs_t h, void* p, size_t bytes, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
 }
 
+// The all-gather + GEMM layer (op == GEMM_RS_OP_AG); see the header.
+static int launch_gather(gemm_rs_t h, const void* A, void* gather, cudaStream_t st) {
+  const long long rank_elems = h->d.M * h->d.K;
+  long long blocks = ((long long)kWorld * rank_elems / 8 + 255) / 256;
+  const long long cap = (long long)h->num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  ag_gather_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint16_t*>(A),
+                                                     static_cast<uint16_t*>(gather), rank_elems);
+  return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
+}
+
+static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out, void* ws,
+                  cudaStream_t st) {
+  const gemm_rs_desc& d = h->d;
+  if (mode == GEMM_RS_CHUNKED) return GEMM_RS_ERR_INVALID_ARG;
+  if (d.M == 0 || d.N == 0) return GEMM_RS_OK;
+  const bool needs_a = mode != GEMM_RS_GEMM_ONLY && d.K > 0;  // GEMM_ONLY reads the buffers
+  const bool needs_w = mode != GEMM_RS_RS_ONLY && d.K > 0;
+  const bool needs_out = mode != GEMM_RS_RS_ONLY;
+  if (!ws) return GEMM_RS_ERR_WORKSPACE;
+  if ((needs_a && !A) || (needs_w && !W) || (needs_out && !out)) return GEMM_RS_ERR_INVALID_ARG;
+  if (!aligned16(ws) || (needs_a && !aligned16(A)) || (needs_w && !aligned16(W)) ||
+      (needs_out && !aligned16(out)))
+    return GEMM_RS_ERR_MISALIGNED;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return GEMM_RS_ERR_INVALID_ARG;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  if (ws != h->last_ws) {  // first use of this workspace: clear counts and control words
+    if (cudaMemsetAsync(wsb + h->lay.flags_off, 0, h->lay.total - h->lay.flags_off, st) !=
+        cudaSuccess)
+      return GEMM_RS_ERR_CUDA;
+    h->last_ws = ws;
+    h->epoch = 0;
+  }
+  h->maps_valid = false;  // the reduce-scatter maps are not kept across ops
+  if (d.K == 0) {  // empty contraction: C is zero, nothing to gather
+    if (mode == GEMM_RS_RS_ONLY) return GEMM_RS_OK;
+    return launch_zero(h, out, (size_t)d.M * d.N * 2, st);
+  }
+  if (mode == GEMM_RS_RS_ONLY) return launch_gather(h, A, wsb, st);
+
+  const uint64_t M = (uint64_t)d.M, K = (uint64_t)d.K, cols = (uint64_t)(d.N / kWorld);
+  const uint64_t shard = M / kWorld;
+  GemmParams& p = h->params;
+  memset(&p, 0, sizeof(p));
+  const bool fused = mode == GEMM_RS_FUSED;
+  // A: the input's row shards (fused: own rows) or the gather buffers
+  bool ok = fused ? make_map(&p.tmap_a, A, K, shard, kWorld, K * 2, K * 2 * shard, kBK, kBM) &&
+                        make_map(&p.tmap_g, wsb, K, M, kWorld, K * 2, K * 2 * M, kBK, kBM)
+                  : make_map(&p.tmap_a, wsb, K, M, kWorld, K * 2, K * 2 * M, kBK, kBM);
+  ok = ok && make_map(&p.tmap_b, W, cols, K, kWorld, cols * 2, cols * 2 * K, 64, kBK);
+  if (!ok) return GEMM_RS_ERR_CUDA;
+  p.stage = static_cast<uint16_t*>(out);  // the epilogue writes C_r = rank r's plane
+  p.plane = (long long)(M * cols);
+  p.out = static_cast<uint16_t*>(out);
+  p.replicas = 1;
+  p.out_stride = p.plane;
+  p.ctrl = reinterpret_cast<uint32_t*>(wsb + h->lay.ctrl_off);
+  p.flags = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
+  p.M = (int)M;
+  p.N = (int)cols;
+  p.Kr = (int)K;
+  p.mt_count = h->mt;
+  p.nt_count = h->nt;
+  p.band = h->band;
+  p.num_kb = h->num_kb;
+  p.unit_rows = h->unit_rows;
+  p.splits = h->splits;
+  p.blocks_per_region = h->blocks_per_region;
+  p.tile_rows = h->tile_rows;
+  p.num_tiles = h->tiles;
+  p.debug_flags = d.debug_flags;
+  p.timeout_ns = d.timeout_ns;
+  p.trace = (d.debug_flags & GEMM_RS_DEBUG_TRACE)
+                ? reinterpret_cast<unsigned long long*>(wsb + h->lay.trace_off)
+                : nullptr;
+  p.ag_src = static_cast<const uint16_t*>(A);
+  p.gather = reinterpret_cast<uint16_t*>(wsb);
+  p.ag_flags = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
+  p.shard_rows = h->shard_rows;
+  p.ag_direct = h->ag_direct;
+  p.chunks_per_shard = h->chunks_per_shard;
+  p.first_round = h->first_round;
+  p.ag_order = 1;
+  p.copy_items = h->copy_items;
+  p.copy_chunk = kCopyChunk;
+  if (fused) {
+    h->epoch += 1;
+    p.ag_target = (uint32_t)h->chunks_per_shard * h->epoch;  // every copied (rank, shard)
+    return launch_gemm_kernel(h->pair, kKindAG, h->grid, 32 * (kGemmWarps + h->reducer_warps),
+                              p, st);
+  }
+  if (mode == GEMM_RS_UNFUSED) {
+    const int rc = launch_gather(h, A, wsb, st);
+    if (rc != GEMM_RS_OK) return rc;
+  }
+  return launch_gemm_kernel(h->pair, kKindGemm, h->grid, 32 * kGemmWarps, p, st);
+}
+
 int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, void* ws,
                 void* stream) {
   if (!h) return GEMM_RS_ERR_INVALID_ARG;
   if (mode < GEMM_RS_FUSED || mode > GEMM_RS_CHUNKED) return GEMM_RS_ERR_INVALID_ARG;
+  if (h->ag) {
+    const int rc = run_ag(h, mode, A, W, out, ws, static_cast<cudaStream_t>(stream));
+    if (rc != GEMM_RS_OK) cudaGetLastError();
+    return rc;
+  }
   const gemm_rs_desc& d = h->d;
   if (d.M == 0 || d.N == 0) return GEMM_RS_OK;  // nothing to read or write
   // A and W hold no element when K == 0: their pointers are not used then.
@@ -600,20 +778,23 @@ extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const
                                 void* ws, void* stream) {
   if (!h) return GEMM_RS_ERR_INVALID_ARG;
   if (mode < GEMM_RS_FUSED || mode > GEMM_RS_CHUNKED) return GEMM_RS_ERR_INVALID_ARG;
-  const bool needs_ab = mode != GEMM_RS_RS_ONLY;
-  const bool needs_out = mode != GEMM_RS_GEMM_ONLY;
+  // which buffers a mode reads and writes (all-gather: GEMM_ONLY reads only the
+  // gather buffers and W, RS_ONLY is the gather: reads A, writes no output)
+  const bool needs_a = h->ag ? mode != GEMM_RS_GEMM_ONLY : mode != GEMM_RS_RS_ONLY;
+  const bool needs_w = mode != GEMM_RS_RS_ONLY;
+  const bool needs_out = h->ag ? mode != GEMM_RS_RS_ONLY : mode != GEMM_RS_GEMM_ONLY;
   const gemm_rs_desc& d = h->d;
   const size_t a_bytes = (size_t)d.M * (size_t)d.K * 2;  // 8 shards of M x K/8
   const size_t w_bytes = (size_t)d.K * (size_t)d.N * 2;  // 8 shards of K/8 x N
   const size_t o_bytes = (size_t)replicas_of(&d) * (size_t)d.M * (size_t)d.N * 2;
-  if ((needs_ab && a_bytes && (!A_host || !A_dev)) || (needs_ab && w_bytes && (!W_host || !W_dev)) ||
+  if ((needs_a && a_bytes && (!A_host || !A_dev)) || (needs_w && w_bytes && (!W_host || !W_dev)) ||
       (needs_out && o_bytes && (!out_host || !out_dev)))
     return GEMM_RS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (needs_ab && a_bytes &&
+  if (needs_a && a_bytes &&
       cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return cudaGetLastError(), GEMM_RS_ERR_CUDA;
-  if (needs_ab && w_bytes &&
+  if (needs_w && w_bytes &&
       cudaMemcpyAsync(W_dev, W_host, w_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return cudaGetLastError(), GEMM_RS_ERR_CUDA;
   int rc = gemm_rs_run(h, mode, A_dev, W_dev, out_dev, ws, stream);
@@ -767,7 +948,7 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.num_items = items_of(blocks, p.blocks_per_region, tail, p.splits);
     p.flag_target = (uint32_t)(kWorld * kEpiWarps);  // counts were just cleared: one run's adds
     p.timeout_ns = kDefaultTimeoutNs;
-    rc = launch_gemm_kernel(kDefaultMmaCtas, true, nd->grid,
+    rc = launch_gemm_kernel(kDefaultMmaCtas, kKindRS, nd->grid,
                             32 * (kGemmWarps + kDefaultReducerWarps), p, st);
     if (rc != GEMM_RS_OK) return rc;
   }

@@ -39,6 +39,13 @@
 
 namespace grs {
 
+// What a launch of gemm_rs_kernel does besides the tile GEMM.
+enum Kind : int {
+  kKindGemm = 0,  // only the GEMM (unfused paths)
+  kKindRS = 1,    // + completion publication and reducer warps (fused reduce-scatter)
+  kKindAG = 2,    // + copy warps gathering A's row shards (fused all-gather + GEMM)
+};
+
 constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
@@ -83,6 +90,7 @@ enum CtrlWord : int {
   kCtrlErrWhere = 4, // which wait gave up
   kCtrlErrWhat = 5,  // region / tile index of that wait
   kCtrlTileTicket = 6, // next GEMM tile to claim
+  kCtrlCopyTicket = 9, // next all-gather copy item to take
   kCtrlCount = 16
 };
 // Every control word, completion count and FIFO slot sits in its own part of
@@ -92,11 +100,29 @@ constexpr int kCtrlWords = kCtrlCount * kCtrlStride;
 constexpr int kFlagStride = 32;   // words: one 128-byte line per block count
 constexpr int kQueueStride = 4;   // 8-byte slots: one 32-byte sector per slot
 enum ErrBits : uint32_t { kErrFlagTimeout = 1u, kErrPipeTimeout = 2u, kErrIncomplete = 4u };
-enum ErrWhere : uint32_t { kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereReducer = 4 };
+enum ErrWhere : uint32_t {
+  kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereReducer = 4, kWhereShard = 5
+};
 
 struct GemmParams {
   CUtensorMap tmap_a;   // A  [8][M][Kr] : dims {Kr, M, 8}, box {64, 128, 1}
   CUtensorMap tmap_b;   // W  [8][Kr][N] : dims {N, Kr, 8}, box {64, 64, 1}
+  // All-gather + GEMM (kKindAG): tmap_a covers the input's row shards
+  // [8][M/8][K] (dims {K, M/8, 8}), tmap_g the gather buffers [8][M][K]
+  // (dims {K, M, 8}; rank r's copy of every shard).  Kr is then the full K and
+  // N the rank's N/8 columns.
+  CUtensorMap tmap_g;
+  const uint16_t* ag_src;  // input row shards, [8][M/8][K]
+  uint16_t* gather;        // gather buffers, [8][M][K]
+  uint32_t* ag_flags;      // copied chunks of shard s in rank r's buffer: ag_flags[(r*8+s)*kFlagStride]
+  uint32_t ag_target;      // chunks per shard x fused all-gather runs so far
+  int shard_rows;          // M / 8
+  int ag_direct;           // own shard read from the input (shard_rows % tile_rows == 0)
+  int chunks_per_shard;
+  int first_round;         // 1 when the own shards are not copied
+  int ag_order;            // tiles in the all-gather order (ag_tile_at), also when unfused
+  long long copy_items;    // copy items of a run
+  long long copy_chunk;    // elements per copy item
   uint16_t* stage;   // rank r's partial of output element (i, j): stage[r * plane + i * N + j]
   long long plane;   // elements from one rank's staging region to the next
   uint16_t* out;
@@ -354,6 +380,77 @@ __device__ __forceinline__ void transpose_granules(uint32_t (&x)[8][4], int t) {
 }
 
 // ---------------------------------------------------------------------------
+// All-gather role (kKindAG): copy warps take copy items from one atomic
+// ticket, in order, rank after rank like the tiles: with R = 8 - first_round
+// rounds per rank, item i is rank r = i / (R * chunks), round k = (i / chunks)
+// mod R + first_round, chunk c: chunk c of shard (r + k) mod 8 into rank r's
+// gather buffer.
+// Copies depend on nothing, so every item is taken by some running warp.
+// After an item, lane 0 publishes it with a release add on (r, s)'s count.
+__device__ __noinline__ void copy_loop(const GemmParams& p, int lane) {
+  const long long shard_elems = (long long)p.shard_rows * p.Kr;
+  const long long per_rank = (long long)(kWorld - p.first_round) * p.chunks_per_shard;
+  while (true) {
+    uint32_t i = 0;
+    if (lane == 0) i = atomicAdd(p.ctrl + kCtrlCopyTicket * kCtrlStride, 1u);
+    i = __shfl_sync(0xffffffffu, i, 0);
+    if ((long long)i >= p.copy_items) break;
+    const int r = (int)(i / per_rank);
+    const long long rem = i % per_rank;
+    const int k = (int)(rem / p.chunks_per_shard) + p.first_round;
+    const long long c = rem % p.chunks_per_shard;
+    const int s = (r + k) % kWorld;
+    const long long e0 = c * p.copy_chunk;
+    long long n = shard_elems - e0;
+    if (n > p.copy_chunk) n = p.copy_chunk;
+    const uint4* src = reinterpret_cast<const uint4*>(p.ag_src + s * shard_elems + e0);
+    uint4* dst = reinterpret_cast<uint4*>(p.gather + (long long)r * p.M * p.Kr + s * shard_elems + e0);
+    // 16 loads of 16 bytes in flight per lane (8 KiB per warp): a copy warp
+    // is latency-bound, and the copies must stay ahead of the tiles
+    constexpr int kU = 16;
+    const long long nv = n / 8;
+    long long v = lane;
+#pragma unroll 1
+    for (; v + 32 * (kU - 1) < nv; v += 32 * kU) {
+      uint4 t[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) t[u] = __ldg(src + v + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) dst[v + 32 * u] = t[u];
+    }
+#pragma unroll 1
+    for (; v < nv; v += 32) dst[v] = __ldg(src + v);
+    __syncwarp();  // the warp's stores are ordered before lane 0's release
+    if (lane == 0 && !((p.debug_flags & 1u) && i == 0)) {  // debug: item 0 never published
+      fence_proxy_async_global();
+      red_release_gpu_add(p.ag_flags + (size_t)(r * kWorld + s) * kFlagStride, 1u);
+    }
+  }
+}
+
+// Producer side of the all-gather: wait (acquire, bounded) until every shard
+// that rows [row_lo, row_hi] of rank r's tile come from is in r's gather
+// buffer; then order the TMA (async proxy) reads after the copies.
+__device__ __forceinline__ bool wait_shards(const GemmParams& p, int r, int row_lo, int row_hi,
+                                            uint64_t limit, volatile uint32_t* abort) {
+  const int s_lo = row_lo / p.shard_rows, s_hi = row_hi / p.shard_rows;
+  for (int s = s_lo; s <= s_hi; ++s) {
+    if (p.ag_direct && s == r) continue;  // read from the input
+    const uint32_t* f = p.ag_flags + (size_t)(r * kWorld + s) * kFlagStride;
+    if ((int)(ld_acquire_gpu(f) - p.ag_target) >= 0) continue;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t sleep_ns = 32;
+    while ((int)(ld_acquire_gpu(f) - p.ag_target) < 0) {
+      if (*abort || globaltimer_ns() - t0 > limit) return false;
+      __nanosleep(sleep_ns);
+      sleep_ns = sleep_ns < 512 ? sleep_ns * 2 : 512;
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // Tile ring: the cluster's first CTA claims tiles from one atomic ticket (so
 // no tile waits for a CTA that is not running) and hands each tile index to
 // every consumer through a small ring in shared memory, mirrored into the
@@ -408,11 +505,13 @@ struct TileRing {
 };
 
 // ---------------------------------------------------------------------------
-// The persistent GEMM kernel.  kFused = true adds completion publication and
-// reducer warps; kCtas selects the tile shape (see TileCfg).
-template <bool kFused, int kCtas>
-__global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps : 0)), 1)
-    gemm_rs_kernel(const __grid_constant__ GemmParams p) {
+// The persistent GEMM kernel.  kKind adds the fused communication role (see
+// Kind); kCtas selects the tile shape (see TileCfg).
+template <int kKind, int kCtas>
+__global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : kMaxReducerWarps)),
+                                  1) gemm_rs_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool kFused = kKind == kKindRS;  // reduce-scatter (or all-reduce) fused
+  constexpr bool kAG = kKind == kKindAG;     // all-gather fused
   using C = TileCfg<kCtas>;
   using Ring = TileRing<kCtas>;
   constexpr int kPair = C::kPair;
@@ -439,6 +538,11 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
   uint32_t* cta_reduced = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc + 8);
   const uint32_t ring_slots = sbase + C::kSmemMisc + 16;
   const uint64_t limit = p.timeout_ns;
+  auto coord = [&](int idx) {
+    return (kAG || p.ag_order)
+               ? ag_tile_at(idx, p.mt_count, p.nt_count, p.shard_rows, C::kTileRows, p.band)
+               : tile_at(idx, p.mt_count, p.nt_count, p.band);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -463,6 +567,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
     fence_proxy_async_shared();
     tma_prefetch_desc(&p.tmap_a);
     tma_prefetch_desc(&p.tmap_b);
+    if (kAG) tma_prefetch_desc(&p.tmap_g);
   }
   if (warp == 1) {
     tmem_alloc<kPair>(smem_u32(tmem_slot), kTmemCols);
@@ -506,9 +611,28 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
           break;
         }
         if (idx < 0) break;
-        const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
+        const TileCoord tc = coord(idx);
         const int m0 = tc.mt * C::kTileRows + (int)cta_rank * kBM;
         const int n0 = tc.nt * kBN + (int)half * C::kBCols;
+        const CUtensorMap* amap = &p.tmap_a;
+        int arow = m0;
+        if constexpr (kAG) {
+          // own rows come from the input; the others once their shards are gathered
+          if (m0 < p.M && p.ag_direct && m0 / p.shard_rows == tc.rank) {
+            arow = m0 - tc.rank * p.shard_rows;
+          } else {
+            amap = &p.tmap_g;
+            if (m0 < p.M &&
+                !wait_shards(p, tc.rank, m0, (m0 + kBM < p.M ? m0 + kBM : p.M) - 1, limit,
+                             cta_abort)) {
+              if (!*cta_abort) {
+                record_error(p, kErrFlagTimeout, kWhereShard, (uint32_t)idx);
+                *cta_abort = 1;
+              }
+              break;
+            }
+          }
+        }
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!bar_wait<kCtas == 4>(bar_empty + 8 * stage, phase ^ 1u, limit, cta_abort)) {
             if (!*cta_abort) {
@@ -523,7 +647,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
           const uint32_t sb = sbase + C::kSmemB + stage * C::kBStage;
           if constexpr (kCtas == 1) {
             mbar_arrive_expect_tx(fb, C::kStage);
-            tma_load_3d(sa, &p.tmap_a, fb, kb * kBK, m0, tc.rank);
+            tma_load_3d(sa, amap, fb, kb * kBK, arow, tc.rank);
 #pragma unroll
             for (int j = 0; j < C::kBBoxes; ++j)
               tma_load_3d(sb + j * C::kBBoxBytes, &p.tmap_b, fb, n0 + 64 * j, kb * kBK, tc.rank);
@@ -531,7 +655,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             // both CTAs' bytes are counted on the leader's barrier
             if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
             const uint32_t fb_leader = mapa_shared(fb, 0);
-            tma_load_3d_pair(sa, &p.tmap_a, fb_leader, kb * kBK, m0, tc.rank);
+            tma_load_3d_pair(sa, amap, fb_leader, kb * kBK, arow, tc.rank);
 #pragma unroll
             for (int j = 0; j < C::kBBoxes; ++j)
               tma_load_3d_pair(sb + j * C::kBBoxBytes, &p.tmap_b, fb_leader, n0 + 64 * j,
@@ -543,7 +667,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
             // CTAs of both pairs that hold that half
             if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
             const uint32_t fb_leader = mapa_shared(fb, mma_leader_rank);
-            tma_load_3d_pair(sa, &p.tmap_a, fb_leader, kb * kBK, m0, tc.rank);
+            tma_load_3d_pair(sa, amap, fb_leader, kb * kBK, arow, tc.rank);
             const uint32_t pair_id = cta_rank >> 1;
             const uint16_t mask = (uint16_t)((1u << half) | (1u << (half + 2)));
             tma_load_3d_pair_multicast(sb + pair_id * C::kBBoxBytes, &p.tmap_b, fb_leader,
@@ -667,7 +791,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
         break;
       }
       if (idx < 0) break;
-      const TileCoord tc = tile_at(idx, p.mt_count, p.nt_count, p.band);
+      const TileCoord tc = coord(idx);
       tc_fence_after();
       const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32 + grp;
       uint16_t* stage_r = p.stage + (size_t)tc.rank * (size_t)p.plane;
@@ -731,8 +855,9 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
     if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
     if (kFused) reducer_loop(p, lane, cta_reduced);  // out of tiles: help with the reduction
   } else {
-    // ------------------------------------------------------------ reducers
+    // ------------------------------------------------- reducers / copy warps
     if (kFused) reducer_loop(p, lane, cta_reduced);
+    if (kAG) copy_loop(p, lane);
   }
 
   if (trace && lane == 0) atomicMax(trace + 3, (unsigned long long)globaltimer_ns());
@@ -754,6 +879,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kFused ? kMaxReducerWarps 
       atomicExch(p.ctrl + kCtrlQueueTail * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlQueueHead * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlTileTicket * kCtrlStride, 0u);
+      atomicExch(p.ctrl + kCtrlCopyTicket * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlAbort * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlDone * kCtrlStride, 0u);
       __threadfence();
@@ -803,6 +929,23 @@ __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restri
 
 
 // Zero fill (empty contraction, K = 0): n16 16-byte vectors.
+// Standalone all-gather of the unfused path: every rank's gather buffer gets
+// all 8 row shards, its own included.  Rank r's buffer [M][K] is the 8 shards
+// one after the other, which is the input's own layout, so it is a copy of
+// the whole input; 16-byte vectors, grid-stride.
+__global__ void __launch_bounds__(256) ag_gather_kernel(const uint16_t* __restrict__ src,
+                                                        uint16_t* __restrict__ gather,
+                                                        long long rank_elems) {
+  const long long per_rank = rank_elems / 8;  // vectors
+  const long long total = (long long)kWorld * per_rank;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(gather);
+#pragma unroll 1
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += stride)
+    d[v] = __ldg(s + v % per_rank);
+}
+
 __global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ p, long long n16) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)

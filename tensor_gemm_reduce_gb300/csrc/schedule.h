@@ -64,6 +64,25 @@ GRS_HD TileCoord tile_at(int64_t idx, int mt_count, int nt_count, int band) {
   return t;
 }
 
+// AllGather + GEMM (mKernel page, section 4: the local shard first, then
+// the other shards, in the order they arrive).  Ranks one after the other
+// (one rank's gathered A and its column shard of W are what L2 keeps);
+// inside a rank, the tile rows are taken from the first tile row of its own
+// shard onwards (wrapping around), in bands of `band` tile rows whose column
+// tiles are walked band by band as in region_at.  The copies bring rank r the
+// shards (r + 1) mod 8, (r + 2) mod 8, ... in the same order.
+GRS_HD TileCoord ag_tile_at(int64_t idx, int mt_count, int nt_count, int shard_rows,
+                            int tile_rows, int band) {
+  const int64_t per_rank = (int64_t)mt_count * nt_count;
+  TileCoord t;
+  t.rank = (int)(idx / per_rank);
+  const Region g = region_at(idx - t.rank * per_rank, mt_count, nt_count, band);
+  const int start = (int)(((int64_t)t.rank * shard_rows) / tile_rows);
+  t.mt = (int)((start + g.mt) % mt_count);
+  t.nt = g.nt;
+  return t;
+}
+
 // Automatic band height, in tile rows of tile_rows output rows: keep the
 // band's rows of A (all ranks, full K) at or under ~32 MiB of the 126 MiB L2,
 // and no taller than the output.

@@ -37,6 +37,8 @@ GEMM_RS_ERR_INCOMPLETE = -9
 NOALLOC_STAGING_BYTES = 32 << 20
 
 FUSED, UNFUSED, GEMM_ONLY, RS_ONLY, CHUNKED = 0, 1, 2, 3, 4
+# layers (gemm_rs_desc.op): GEMM then reduce-scatter / all-reduce, or all-gather then GEMM
+OP_RS, OP_AG = 0, 1
 MODES = {"fused": FUSED, "unfused": UNFUSED, "gemm_only": GEMM_ONLY, "rs_only": RS_ONLY,
          "chunked": CHUNKED}
 
@@ -60,6 +62,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("mma_ctas", ctypes.c_int32),
         ("chunks", ctypes.c_int32),
         ("replicas", ctypes.c_int32),
+        ("op", ctypes.c_int32),
     ]
 
 
@@ -84,6 +87,9 @@ class gemm_rs_info(ctypes.Structure):
         ("trace_offset", ctypes.c_int64),
         ("chunks", ctypes.c_int32),
         ("replicas", ctypes.c_int32),
+        ("op", ctypes.c_int32),
+        ("ag_direct", ctypes.c_int32),
+        ("copy_items", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -160,9 +166,9 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          mma_ctas=0, chunks=0, replicas=0, world=WORLD):
+          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas, chunks, replicas)
+                        debug_flags, mma_ctas, chunks, replicas, op)
 
 
 # ----------------------------------------------------------------------------
@@ -240,16 +246,34 @@ class Plan:
 
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
-                 mma_ctas: int = 0, chunks: int = 0, replicas: int = 0):
+                 mma_ctas: int = 0, chunks: int = 0, replicas: int = 0, op: int = OP_RS):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.replicas = max(1, int(replicas))
+        self.op = int(op)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
-                          timeout_ns, debug_flags, mma_ctas, chunks, replicas)
+                          timeout_ns, debug_flags, mma_ctas, chunks, replicas, op)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property
+    def a_shape(self):
+        """[8][M][K/8] (row-parallel: K shards) or [8][M/8][K] (all-gather: row shards)."""
+        if self.op == OP_AG:
+            return (WORLD, self.M // WORLD, self.K)
+        return (WORLD, self.M, self.K // WORLD)
+
+    @property
+    def w_shape(self):
+        """[8][K/8][N] (row-parallel) or [8][K][N/8] (all-gather: column shards)."""
+        if self.op == OP_AG:
+            return (WORLD, self.K, self.N // WORLD)
+        return (WORLD, self.K // WORLD, self.N)
+
+    @property
     def out_shape(self):
-        """[M][N] (reduce-scatter) or [8][M][N] (all-reduce: one copy per rank)."""
+        """[M][N] (reduce-scatter), [8][M][N] (all-reduce: one copy per rank) or
+        [8][M][N/8] (all-gather + GEMM: rank r's column block)."""
+        if self.op == OP_AG:
+            return (WORLD, self.M, self.N // WORLD)
         return (self.M, self.N) if self.replicas == 1 else (self.replicas, self.M, self.N)
 
     @property
@@ -275,9 +299,8 @@ class Plan:
 
     def run(self, A, W, out, workspace, mode: int = FUSED, stream=None) -> None:
         import torch
-        Kr = self.K // WORLD
-        a = self._check(A, (WORLD, self.M, Kr), "A")
-        w = self._check(W, (WORLD, Kr, self.N), "W")
+        a = self._check(A, self.a_shape, "A")
+        w = self._check(W, self.w_shape, "W")
         o = self._check(out, self.out_shape, "out")
         if workspace is None or workspace.numel() * workspace.element_size() < self.workspace_bytes:
             raise ValueError("workspace missing or too small")
@@ -291,14 +314,13 @@ class Plan:
         """Host tensors in (pinned for asynchronous copies), host tensor out; the
         copies and the run are enqueued on one stream by the library."""
         import torch
-        Kr = self.K // WORLD
-        for t, shape, name in ((A_host, (WORLD, self.M, Kr), "A_host"),
-                               (W_host, (WORLD, Kr, self.N), "W_host"),
+        for t, shape, name in ((A_host, self.a_shape, "A_host"),
+                               (W_host, self.w_shape, "W_host"),
                                (out_host, self.out_shape, "out_host")):
             if t.dtype != torch.bfloat16 or tuple(t.shape) != shape or t.is_cuda or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous host bf16 tensor of shape {shape}")
-        a = self._check(A, (WORLD, self.M, Kr), "A")
-        w = self._check(W, (WORLD, Kr, self.N), "W")
+        a = self._check(A, self.a_shape, "A")
+        w = self._check(W, self.w_shape, "W")
         o = self._check(out, self.out_shape, "out")
         if workspace is None or workspace.numel() * workspace.element_size() < self.workspace_bytes:
             raise ValueError("workspace missing or too small")

@@ -21,6 +21,14 @@ Recipe (identical bits on every machine):
   * both rounded once to bf16 (round to nearest even);
   * A_shards = A reshaped to [8][M][K/8] (rank-major, K/8 contiguous),
     W_shards = W reshaped to [8][K/8][N] (rank-major, N contiguous).
+
+All-gather + GEMM workloads (op "ag": the column-parallel partner layer,
+FLUX page abstract and Figure 1, mKernel page section 4) draw A and W the
+same way and shard them the other way round: rank r holds rows
+[r*M/8, (r+1)*M/8) of A ([8][M/8][K]) and columns [r*N/8, (r+1)*N/8) of W
+([8][K][N/8]).  Shapes: the Llama-3 70B attention QKV projection (N = 8192 +
+2 * 1024) and the FLUX page's Figure 4 shapes, (n, k) = (49152, 12288) for
+the all-gather and (12288, 49152) for the reduce-scatter, m from 1024 to 8192.
 """
 from __future__ import annotations
 
@@ -40,6 +48,7 @@ class Workload:
     K: int
     seed: int
     outliers: bool = False
+    op: str = "rs"  # "rs": row-parallel (GEMM + reduce-scatter); "ag": all-gather + GEMM
 
     @property
     def Kr(self) -> int:
@@ -68,6 +77,14 @@ def _registry() -> List[Workload]:
     for i, m in enumerate((2048, 32768)):
         w.append(Workload(f"mixtral_8x22b_down_proj_m{m}", m, 6144, 16384,
                           seed=3000 + i))
+    # the FLUX page's Figure 4 reduce-scatter shape
+    for i, m in enumerate((1024, 2048, 4096, 8192)):
+        w.append(Workload(f"flux_fig4_rs_m{m}", m, 12288, 49152, seed=5200 + i))
+    # all-gather + GEMM: tiny, Llama-3-70B QKV projection, FLUX Figure 4's shape
+    w.append(Workload("tiny_ag", 128, 512, 1024, seed=100, op="ag"))
+    w.append(Workload("llama3_70b_qkv_m2048", 2048, 10240, 8192, seed=5000, op="ag"))
+    for i, m in enumerate((1024, 2048, 4096, 8192)):
+        w.append(Workload(f"flux_fig4_ag_m{m}", m, 49152, 12288, seed=5100 + i, op="ag"))
     # the full sweep
     for j, (n, k) in enumerate(((8192, 8192), (8192, 28672), (6144, 6144), (6144, 16384))):
         for i, m in enumerate((512, 2048, 8192, 32768)):
@@ -114,13 +131,24 @@ def shard(A_bits: np.ndarray, W_bits: np.ndarray, world: int = WORLD):
     return A_sh, W_sh
 
 
+def shard_ag(A_bits: np.ndarray, W_bits: np.ndarray, world: int = WORLD):
+    """Split A[M][K] by rows and W[K][N] by columns: ([8][M/8][K], [8][K][N/8])."""
+    M, K = A_bits.shape
+    K2, N = W_bits.shape
+    assert K == K2 and M % world == 0 and N % world == 0
+    A_sh = np.ascontiguousarray(A_bits.reshape(world, M // world, K))
+    W_sh = np.ascontiguousarray(W_bits.reshape(K, world, N // world).transpose(1, 0, 2))
+    return A_sh, W_sh
+
+
 def make_inputs(w: Workload):
-    """Seeded shards for a registered workload: (A_sh[8][M][Kr], W_sh[8][Kr][N]) uint16."""
+    """Seeded shards for a registered workload (uint16 bf16 patterns): for "rs"
+    (A_sh[8][M][K/8], W_sh[8][K/8][N]), for "ag" (A_sh[8][M/8][K], W_sh[8][K][N/8])."""
     A, W = draw_full(w.M, w.N, w.K, w.seed, w.outliers)
-    return shard(A, W)
+    return shard_ag(A, W) if w.op == "ag" else shard(A, W)
 
 
-def make_shape_inputs(M: int, N: int, K: int, seed: int, outliers: bool = False):
+def make_shape_inputs(M: int, N: int, K: int, seed: int, outliers: bool = False, op: str = "rs"):
     """Seeded shards for an arbitrary shape (test cases)."""
     A, W = draw_full(M, N, K, seed, outliers)
-    return shard(A, W)
+    return shard_ag(A, W) if op == "ag" else shard(A, W)

@@ -44,6 +44,9 @@ def _create(**kw):
     (dict(chunks=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(chunks=65), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(replicas=2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(op=2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(op=G.OP_AG, replicas=8), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(op=G.OP_AG, N=264), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(replicas=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(N=12), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
@@ -121,3 +124,22 @@ def test_auto_band_keeps_a_rows_within_budget(lib, ctas):
         band = band if band is not None else mt
         assert 1 <= band <= mt
         assert band == mt or band * rows * K * 2 <= 32 << 20
+
+
+@pytest.mark.parametrize("ctas", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(2048, 10240, 8192), (392, 1536, 1600), (128, 512, 1024)])
+def test_ag_schedule_walks_from_own_shard(lib, M, N, K, ctas):
+    """All-gather + GEMM order (mKernel page, section 4): every rank tile once,
+    rank after rank; each rank starts at the tile row holding its own shard."""
+    d = G._desc(M, N, K, mma_ctas=ctas, op=G.OP_AG)
+    rows = 128 * ctas
+    mt, nt = (M + rows - 1) // rows, (N // 8 + 255) // 256
+    seen = []
+    for i in range(8 * mt * nt):
+        seen.append(tuple(G.gemm_rs_schedule(d, i)))
+    assert len(set(seen)) == 8 * mt * nt
+    per_rank = mt * nt
+    for r in range(8):
+        mine = seen[r * per_rank:(r + 1) * per_rank]  # ranks one after the other
+        assert {t[0] for t in mine} == {r}
+        assert mine[0][1] == (r * (M // 8)) // rows and mine[0][2] == 0  # own shard first

@@ -364,3 +364,62 @@ def test_allreduce_every_rank_holds_the_brute_force_sum(M, N, K, seed):
     for s_, sl in enumerate(oracle.slices(rs)):
         h = M // 8
         assert np.array_equal(out8[(s_ + 3) % 8][s_ * h:(s_ + 1) * h], sl)
+
+
+# ---------------------------------------------------------------------------
+# All-gather + GEMM (the column-parallel partner layer)
+
+def _ag_brute_force(A_sh, W_sh):
+    """Exact products of the gathered A with each column shard, rounded once."""
+    A = [[Fraction(float(v)) for v in row] for a in A_sh for row in oracle.bf16_from_bits(a)]
+    out = []
+    for w in W_sh:
+        Wv = [[Fraction(float(v)) for v in row] for row in oracle.bf16_from_bits(w)]
+        K, n = len(Wv), len(Wv[0])
+        out.append([[float(rbf16(sum((A[i][k] * Wv[k][j] for k in range(K)), Fraction(0))))
+                     for j in range(n)] for i in range(len(A))])
+    return np.array(out)
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(16, 16, 8, 51), (8, 64, 24, 52), (24, 8, 40, 53)])
+def test_ag_gemm_matches_brute_force(M, N, K, seed):
+    A_sh, W_sh = workloads.make_shape_inputs(M, N, K, seed, op="ag")
+    C, ref = oracle.ag_gemm(A_sh, W_sh)
+    assert C.shape == (8, M, N // 8)
+    assert np.array_equal(C, _ag_brute_force(A_sh, W_sh))
+
+
+def test_ag_gemm_column_blocks_form_one_product():
+    """The ranks' column blocks side by side are the single rounding of the
+    unsharded product A W (numpy's float64 matmul of the full matrices)."""
+    M, N, K = 48, 128, 256
+    A, W = workloads.draw_full(M, N, K, seed=54)
+    A_sh, W_sh = workloads.shard_ag(A, W)
+    C, _ = oracle.ag_gemm(A_sh, W_sh)
+    full = oracle.bf16_round(oracle.bf16_from_bits(A) @ oracle.bf16_from_bits(W))
+    assert np.array_equal(np.concatenate(list(C), axis=1), full)
+
+
+def test_ag_gemm_identity_and_single_shard():
+    M, K = 64, 64
+    A, _ = workloads.draw_full(M, K, K, seed=55)
+    A_sh, W_sh = workloads.shard_ag(A, oracle.bf16_to_bits(np.eye(K)))
+    C, _ = oracle.ag_gemm(A_sh, W_sh)
+    Av = oracle.bf16_from_bits(A)
+    for r in range(8):
+        assert np.array_equal(C[r], Av[:, r * K // 8:(r + 1) * K // 8])
+    # only shard 3 non-zero: every rank's rows outside shard 3 are zero
+    A2 = A_sh.copy()
+    A2[[q for q in range(8) if q != 3]] = 0
+    C2, _ = oracle.ag_gemm(A2, W_sh)
+    h = M // 8
+    assert np.count_nonzero(C2[:, :3 * h]) == 0 and np.count_nonzero(C2[:, 4 * h:]) == 0
+    assert np.array_equal(C2[:, 3 * h:4 * h], C[:, 3 * h:4 * h])
+
+
+def test_ag_gemm_rows_subset():
+    A_sh, W_sh = workloads.make_shape_inputs(64, 128, 128, 56, op="ag")
+    C, _ = oracle.ag_gemm(A_sh, W_sh)
+    rows = [0, 7, 8, 33, 63]
+    Cr, _ = oracle.ag_gemm_rows(A_sh, W_sh, rows)
+    assert np.array_equal(Cr, C[:, rows])
