@@ -134,6 +134,9 @@ typedef struct gemm_rs_desc {
                              all-reduce, out is [8][M][N] and copy r is virtual rank r's
                              full sum (bitwise the reduce-scatter output) */
   int32_t op;             /* GEMM_RS_OP_RS (0) or GEMM_RS_OP_AG (1) */
+  int32_t adaptive;       /* FUSED reduce-scatter: 1 = an on-GPU controller sets how many of
+                             each CTA's reducer warps take items, from cycle and progress
+                             counters (mKernel page, section 3.2); 0 = all of them */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -266,6 +269,38 @@ int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, int64_t M, in
 
 /* Release the plan (host state only; device buffers stay the caller's). */
 int gemm_rs_destroy(gemm_rs_t plan);
+
+/*
+ * Auto-tuning (FLUX page, TL;DR: tile swizzling and auto-tuning; mKernel page,
+ * section 5.5: the best share of communication workers varies with the kernel
+ * and the shape).  The candidates for d's problem are d with, in turn:
+ *   reduce-scatter / all-reduce: mma_ctas in {2, 1} x reducer_warps in {2, 4, 6}
+ *     x unit_rows in {16, 32};
+ *   all-gather: mma_ctas in {2, 1} x copy warps (reducer_warps) in {1, 2, 4};
+ * every other field as in d.  gemm_rs_tune_candidates writes up to `max` of them
+ * to `cands` (may be NULL), sets *count, and *workspace_bytes (may be NULL) to
+ * the largest workspace any of them needs.  Host only; checks d first.
+ */
+#define GEMM_RS_TUNE_MAX 16
+int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max, int* count,
+                            size_t* workspace_bytes);
+
+/*
+ * Time every candidate of gemm_rs_tune_candidates in `mode` on the caller's
+ * buffers (as gemm_rs_run; ws of ws_bytes >= the candidates' largest
+ * workspace) and return the fastest in *best with its time in *best_us.
+ * Each candidate runs 3 warm-up launches, then `rounds` rounds in which every
+ * candidate is timed over `iters` back-to-back runs with CUDA events on
+ * `stream` (interleaved, so drifting clocks affect all alike); a candidate's
+ * time is the median over rounds of its per-run mean.  times_us (may be NULL,
+ * GEMM_RS_TUNE_MAX entries) receives every candidate's time, in candidate
+ * order; a candidate that cannot be created or whose run fails gets -1 and is
+ * skipped.  The output and workspace hold the last candidate's run afterwards.
+ * Synchronises `stream`.
+ */
+int gemm_rs_tune(const gemm_rs_desc* d, int mode, const void* A, const void* W, void* out,
+                 void* ws, size_t ws_bytes, int iters, int rounds, void* stream,
+                 gemm_rs_desc* best, float* best_us, float* times_us);
 
 /* Static text for a status code. */
 const char* gemm_rs_strerror(int code);

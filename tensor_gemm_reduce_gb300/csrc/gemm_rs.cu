@@ -71,6 +71,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->chunks < 0 || d->chunks > kMaxChunks) return GEMM_RS_ERR_INVALID_ARG;
   if (d->replicas != 0 && d->replicas != 1 && d->replicas != kWorld) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op != GEMM_RS_OP_RS && d->op != GEMM_RS_OP_AG) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->adaptive != 0 && d->adaptive != 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op == GEMM_RS_OP_AG && d->replicas > 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
@@ -425,6 +426,132 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   return GEMM_RS_OK;
 }
 
+int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max, int* count,
+                            size_t* workspace_bytes) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!count) return GEMM_RS_ERR_INVALID_ARG;
+  const bool ag = d->op == GEMM_RS_OP_AG;
+  static const int kCtas[2] = {2, 1};
+  static const int kWarpsRs[3] = {2, 4, 6}, kWarpsAg[3] = {1, 2, 4};
+  static const int kUnits[2] = {16, 32};
+  int n = 0;
+  size_t ws_max = 0;
+  for (int c = 0; c < 2; ++c)
+    for (int w = 0; w < 3; ++w)
+      for (int u = 0; u < (ag ? 1 : 2); ++u) {
+        gemm_rs_desc e = *d;
+        e.mma_ctas = kCtas[c];
+        e.reducer_warps = ag ? kWarpsAg[w] : kWarpsRs[w];
+        if (!ag) e.unit_rows = kUnits[u];
+        if (cands && n < max) cands[n] = e;
+        // the workspace size depends only on the shape, tile shape and unit rows
+        const int tile_rows = kBM * e.mma_ctas;
+        size_t bytes;
+        if (ag) {
+          bytes = layout_ag(e.M, e.K).total;
+        } else {
+          const int mt = (int)((e.M + tile_rows - 1) / tile_rows), nt = (int)((e.N + kBN - 1) / kBN);
+          const int bpr = tile_rows / kBM, splits = kBM / e.unit_rows;
+          const long long blocks = (long long)mt * nt * bpr;
+          // the largest item count: no tail region (the tail's 4-row items are more)
+          const long long items = (long long)mt * nt * bpr * (kBM / 4);
+          (void)splits;
+          bytes = layout_for(e.M, e.N, blocks, items).total;
+        }
+        if (bytes > ws_max) ws_max = bytes;
+        ++n;
+      }
+  *count = n;
+  if (workspace_bytes) *workspace_bytes = ws_max;
+  return GEMM_RS_OK;
+}
+
+int gemm_rs_tune(const gemm_rs_desc* d, int mode, const void* A, const void* W, void* out,
+                 void* ws, size_t ws_bytes, int iters, int rounds, void* stream,
+                 gemm_rs_desc* best, float* best_us, float* times_us) {
+  gemm_rs_desc cands[GEMM_RS_TUNE_MAX];
+  int n = 0;
+  int rc = gemm_rs_tune_candidates(d, cands, GEMM_RS_TUNE_MAX, &n, nullptr);
+  if (rc) return rc;
+  if (!best || iters < 1 || rounds < 1 || !ws) return GEMM_RS_ERR_INVALID_ARG;
+  if (n > GEMM_RS_TUNE_MAX) n = GEMM_RS_TUNE_MAX;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gemm_rs_t plans[GEMM_RS_TUNE_MAX] = {};
+  float per_round[GEMM_RS_TUNE_MAX][16];
+  bool ok[GEMM_RS_TUNE_MAX];
+  if (rounds > 16) rounds = 16;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    cudaGetLastError();
+    if (e0) cudaEventDestroy(e0);
+    return GEMM_RS_ERR_CUDA;
+  }
+  // Plans share the caller's workspace: before a plan's launches, make it
+  // clear the counters and restart its epoch (another plan advanced them).
+  auto run_plan = [&](int i) {
+    plans[i]->last_ws = nullptr;
+    return gemm_rs_run(plans[i], mode, A, W, out, ws, stream);
+  };
+  for (int i = 0; i < n; ++i) {
+    size_t need = 0;
+    ok[i] = gemm_rs_create(&cands[i], &plans[i], &need) == GEMM_RS_OK && need <= ws_bytes;
+    for (int w = 0; ok[i] && w < 3; ++w) ok[i] = run_plan(i) == GEMM_RS_OK;
+    if (ok[i]) ok[i] = gemm_rs_status(plans[i], stream) == GEMM_RS_OK;
+  }
+  for (int r = 0; r < rounds; ++r)
+    for (int i = 0; i < n; ++i) {
+      if (!ok[i]) continue;
+      plans[i]->last_ws = nullptr;
+      if (gemm_rs_run(plans[i], mode, A, W, out, ws, stream) != GEMM_RS_OK) {  // clears, warms
+        ok[i] = false;
+        continue;
+      }
+      cudaEventRecord(e0, st);
+      bool good = true;
+      for (int k = 0; k < iters && good; ++k)
+        good = gemm_rs_run(plans[i], mode, A, W, out, ws, stream) == GEMM_RS_OK;
+      cudaEventRecord(e1, st);
+      float ms = 0.f;
+      if (!good || cudaEventSynchronize(e1) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess ||
+          gemm_rs_status(plans[i], stream) != GEMM_RS_OK) {
+        cudaGetLastError();
+        ok[i] = false;
+        continue;
+      }
+      per_round[i][r] = ms * 1000.f / (float)iters;
+    }
+  int bi = -1;
+  float bt = 0.f;
+  for (int i = 0; i < n; ++i) {
+    float t = -1.f;
+    if (ok[i]) {  // median over rounds (insertion sort of a few values)
+      float v[16];
+      for (int r = 0; r < rounds; ++r) v[r] = per_round[i][r];
+      for (int a = 1; a < rounds; ++a)
+        for (int b = a; b > 0 && v[b] < v[b - 1]; --b) {
+          const float x = v[b];
+          v[b] = v[b - 1];
+          v[b - 1] = x;
+        }
+      t = v[rounds / 2];
+      if (bi < 0 || t < bt) {
+        bi = i;
+        bt = t;
+      }
+    }
+    if (times_us) times_us[i] = t;
+    if (plans[i]) gemm_rs_destroy(plans[i]);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (bi < 0) return GEMM_RS_ERR_CUDA;
+  *best = cands[bi];
+  if (best_us) *best_us = bt;
+  return GEMM_RS_OK;
+}
+
 int gemm_rs_destroy(gemm_rs_t h) {
   if (!h) return GEMM_RS_OK;
   if (h->side) {
@@ -704,6 +831,8 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     p.trace = (d.debug_flags & GEMM_RS_DEBUG_TRACE)
                   ? reinterpret_cast<unsigned long long*>(wsb + h->lay.trace_off)
                   : nullptr;
+    p.adaptive = d.adaptive;
+    p.reducer_warps = h->reducer_warps;
     h->map_A = a;
     h->map_W = w;
     h->map_ws = ws;

@@ -91,6 +91,7 @@ enum CtrlWord : int {
   kCtrlErrWhat = 5,  // region / tile index of that wait
   kCtrlTileTicket = 6, // next GEMM tile to claim
   kCtrlCopyTicket = 9, // next all-gather copy item to take
+  kCtrlTarget = 10,    // adaptive: reducer warps per CTA that take items (0 = all)
   kCtrlCount = 16
 };
 // Every control word, completion count and FIFO slot sits in its own part of
@@ -156,6 +157,10 @@ struct GemmParams {
   // discarded from L2 (never written back).  Needs N % 64 == 0 so that no
   // 128-byte line holds data of two reduce units.
   uint32_t staging_in_l2;
+  // Adaptive reducer share (mKernel page, section 3.2): a controller thread
+  // publishes how many of each CTA's reducer warps take items; the others wait.
+  int adaptive;
+  int reducer_warps;
   int tile_rows;  // rows of a region: 128 (one CTA per MMA) or 256 (a CTA pair)
   unsigned long long timeout_ns;
   // Debug timeline (null unless asked for): per CTA, global-timer stamps
@@ -321,11 +326,73 @@ __device__ __forceinline__ void reduce_item(const GemmParams& p, int item, int l
   if (row < row_end) reduce_rows<1>(p, plane, row, col, active, drop);
 }
 
+// Adaptive reducer share (mKernel page, section 3.2: a controller estimates
+// the roles' costs from cycle counters and sets the number of communication
+// workers so that the predicted completion times are equal).  Run by one
+// thread (CTA 0's first reducer warp) after each of its items: with tau its
+// own cycles per item (moving average), rate the tiles claimed per cycle
+// (moving average of the ticket's advance), W the items not yet taken and T
+// the tiles not yet claimed, the reduction keeps pace with the GEMM if each
+// CTA runs w >= W * tau * rate / (grid * T) reducer warps; one more is added
+// as margin, and all of them once every tile is claimed.
+struct Controller {
+  float tau = 0.f, rate = 0.f;
+  long long last_clock = 0;
+  uint32_t last_ticket = 0;
+  __device__ void update(const GemmParams& p, long long item_cycles) {
+    const long long now = clock64();
+    const uint32_t ticket = ld_volatile_u32(p.ctrl + kCtrlTileTicket * kCtrlStride);
+    const uint32_t head = ld_volatile_u32(p.ctrl + kCtrlQueueHead * kCtrlStride);
+    tau = tau == 0.f ? (float)item_cycles : 0.8f * tau + 0.2f * (float)item_cycles;
+    if (last_clock != 0 && now > last_clock && ticket >= last_ticket) {
+      const float r = (float)(ticket - last_ticket) / (float)(now - last_clock);
+      rate = rate == 0.f ? r : 0.8f * rate + 0.2f * r;
+    }
+    last_clock = now;
+    last_ticket = ticket;
+    const long long tiles_left = p.num_tiles - (long long)ticket;
+    int w = p.reducer_warps;
+    if (tiles_left > 0 && rate > 0.f) {
+      const float items_left = (float)(p.num_items - (long long)head);
+      const float need = items_left * tau * rate / ((float)gridDim.x * (float)tiles_left);
+      w = (int)ceilf(need) + 1;
+      if (w < 1) w = 1;
+      if (w > p.reducer_warps) w = p.reducer_warps;
+    }
+    atomicExch(p.ctrl + kCtrlTarget * kCtrlStride, (uint32_t)w);
+  }
+};
+
+// A reducer warp above the published share waits here (bounded): false once
+// every item is taken or the run is aborting, so the warp can stop.
+__device__ __forceinline__ bool wait_for_share(const GemmParams& p, int my_idx, int lane) {
+  int go = 1;
+  if (lane == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      const uint32_t target = ld_volatile_u32(p.ctrl + kCtrlTarget * kCtrlStride);
+      if (target == 0 || my_idx < (int)target) break;
+      if ((long long)ld_volatile_u32(p.ctrl + kCtrlQueueHead * kCtrlStride) >= p.num_items ||
+          ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride) || globaltimer_ns() - t0 > p.timeout_ns) {
+        go = 0;
+        break;
+      }
+      __nanosleep(1000);
+    }
+  }
+  return __shfl_sync(0xffffffffu, go, 0) != 0;
+}
+
 // Reducer role: take FIFO positions until every item of the run is taken.
 // Items done are counted in the CTA's shared counter (added to the run's
-// total once, when the CTA ends).
-__device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_t* cta_reduced) {
+// total once, when the CTA ends).  my_idx: the warp's index among the CTA's
+// reducer warps (-1 for epilogue warps that joined: never held back).
+__device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_t* cta_reduced,
+                                          int my_idx) {
+  const bool controller = p.adaptive && my_idx == 0 && blockIdx.x == 0 && lane == 0;
+  Controller ctl;
   while (true) {
+    if (p.adaptive && my_idx > 0 && !wait_for_share(p, my_idx, lane)) break;
     const int item = queue_pop(p, lane);
     if (item == -1) break;
     if (item == -2) {
@@ -333,9 +400,11 @@ __device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_
         record_error(p, kErrFlagTimeout, kWhereReducer, 0xFFFFFFFFu);
       break;
     }
+    const long long c0 = controller ? clock64() : 0;
     reduce_item(p, item, lane);
     __syncwarp();
     if (lane == 0) atomicAdd(cta_reduced, 1u);
+    if (controller) ctl.update(p, clock64() - c0);
   }
 }
 
@@ -853,10 +922,10 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
       if (acc == 0) acc_phase ^= 1u;
     }
     if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
-    if (kFused) reducer_loop(p, lane, cta_reduced);  // out of tiles: help with the reduction
+    if (kFused) reducer_loop(p, lane, cta_reduced, -1);  // out of tiles: help with the reduction
   } else {
     // ------------------------------------------------- reducers / copy warps
-    if (kFused) reducer_loop(p, lane, cta_reduced);
+    if (kFused) reducer_loop(p, lane, cta_reduced, warp - kGemmWarps);
     if (kAG) copy_loop(p, lane);
   }
 
@@ -880,6 +949,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
       atomicExch(p.ctrl + kCtrlQueueHead * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlTileTicket * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlCopyTicket * kCtrlStride, 0u);
+      atomicExch(p.ctrl + kCtrlTarget * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlAbort * kCtrlStride, 0u);
       atomicExch(p.ctrl + kCtrlDone * kCtrlStride, 0u);
       __threadfence();

@@ -63,6 +63,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("chunks", ctypes.c_int32),
         ("replicas", ctypes.c_int32),
         ("op", ctypes.c_int32),
+        ("adaptive", ctypes.c_int32),
     ]
 
 
@@ -122,6 +123,14 @@ _SIGS = {
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_void_p, ctypes.c_void_p]),
     "gemm_rs_destroy": (ctypes.c_int, [ctypes.c_void_p]),
+    "gemm_rs_tune_candidates": (ctypes.c_int, [ctypes.POINTER(gemm_rs_desc), ctypes.POINTER(gemm_rs_desc),
+                                               ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                               ctypes.POINTER(ctypes.c_size_t)]),
+    "gemm_rs_tune": (ctypes.c_int, [ctypes.POINTER(gemm_rs_desc), ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.POINTER(gemm_rs_desc), ctypes.POINTER(ctypes.c_float),
+                                    ctypes.POINTER(ctypes.c_float)]),
     "gemm_rs_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -166,9 +175,9 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, world=WORLD):
+          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, adaptive=0, world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas, chunks, replicas, op)
+                        debug_flags, mma_ctas, chunks, replicas, op, adaptive)
 
 
 # ----------------------------------------------------------------------------
@@ -246,12 +255,13 @@ class Plan:
 
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
-                 mma_ctas: int = 0, chunks: int = 0, replicas: int = 0, op: int = OP_RS):
+                 mma_ctas: int = 0, chunks: int = 0, replicas: int = 0, op: int = OP_RS,
+                 adaptive: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.replicas = max(1, int(replicas))
         self.op = int(op)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
-                          timeout_ns, debug_flags, mma_ctas, chunks, replicas, op)
+                          timeout_ns, debug_flags, mma_ctas, chunks, replicas, op, adaptive)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property
@@ -371,3 +381,56 @@ def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Pl
         workspace = plan.new_workspace(A.device)
     plan.run(A, W, out, workspace, mode)
     return out, plan, workspace
+
+
+# ----------------------------------------------------------------------------
+# auto-tuning
+# ----------------------------------------------------------------------------
+
+TUNE_MAX = 16
+_DESC_KW = ("reducer_warps", "grid", "band_m", "unit_rows", "timeout_ns", "debug_flags",
+            "mma_ctas", "chunks", "replicas", "op", "adaptive")
+
+
+def tune_candidates(desc: gemm_rs_desc):
+    """(list of candidate descs, workspace bytes that fits every one of them)."""
+    lib = load_library()
+    arr = (gemm_rs_desc * TUNE_MAX)()
+    n = ctypes.c_int()
+    ws = ctypes.c_size_t()
+    rc = lib.gemm_rs_tune_candidates(ctypes.byref(desc), arr, TUNE_MAX, ctypes.byref(n),
+                                     ctypes.byref(ws))
+    if rc != GEMM_RS_OK:
+        raise GemmRSError(rc, "gemm_rs_tune_candidates")
+    return [arr[i] for i in range(min(n.value, TUNE_MAX))], ws.value
+
+
+def desc_kwargs(desc: gemm_rs_desc) -> dict:
+    """Plan(...) keyword arguments of a descriptor."""
+    return {k: getattr(desc, k) for k in _DESC_KW}
+
+
+def tune(M, N, K, A, W, out, mode: int = FUSED, iters: int = 10, rounds: int = 3, stream=None,
+         workspace=None, **plan_kw):
+    """Time the tuning candidates of (M, N, K, plan_kw) on these buffers.
+
+    Returns (best Plan keyword arguments, best time in us, [(kwargs, us), ...]).
+    """
+    import torch
+    desc = _desc(int(M), int(N), int(K), **plan_kw)
+    cands, ws_bytes = tune_candidates(desc)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=A.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    best = gemm_rs_desc()
+    best_us = ctypes.c_float()
+    times = (ctypes.c_float * TUNE_MAX)()
+    rc = load_library().gemm_rs_tune(ctypes.byref(desc), int(mode), A.data_ptr(), W.data_ptr(),
+                                     out.data_ptr(), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), int(iters),
+                                     int(rounds), s.cuda_stream, ctypes.byref(best),
+                                     ctypes.byref(best_us), times)
+    if rc != GEMM_RS_OK:
+        raise GemmRSError(rc, "gemm_rs_tune")
+    table = [(desc_kwargs(c), float(times[i])) for i, c in enumerate(cands)]
+    return desc_kwargs(best), float(best_us.value), table

@@ -143,3 +143,20 @@ def test_ag_schedule_walks_from_own_shard(lib, M, N, K, ctas):
         mine = seen[r * per_rank:(r + 1) * per_rank]  # ranks one after the other
         assert {t[0] for t in mine} == {r}
         assert mine[0][1] == (r * (M // 8)) // rows and mine[0][2] == 0  # own shard first
+
+
+@pytest.mark.parametrize("op", [0, 1])
+def test_tune_candidates_and_their_workspace(lib, op):
+    """The tuner's candidate set (host only): the requested plan with the tile
+    shape and the number of communication warps (and unit rows) varied, and one
+    workspace size that fits every candidate."""
+    d = G._desc(1024, 2048, 4096, op=op, timeout_ns=7)
+    cands, ws = G.tune_candidates(d)
+    assert len(cands) == (12 if op == 0 else 6)
+    assert len({(c.mma_ctas, c.reducer_warps, c.unit_rows) for c in cands}) == len(cands)
+    assert all(c.M == 1024 and c.N == 2048 and c.K == 4096 and c.op == op and c.timeout_ns == 7
+               for c in cands)
+    staging = 8 * 1024 * (2048 if op == 0 else 4096) * 2
+    assert ws > staging
+    with pytest.raises(G.GemmRSError):
+        G.tune_candidates(G._desc(100, 256, 512))

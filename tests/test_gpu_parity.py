@@ -16,7 +16,7 @@ import torch
 import oracle
 from tensor_gemm_reduce_gb300 import gemm_rs as G
 from tensor_gemm_reduce_gb300 import workloads
-from gpu_helpers import (Case, TOL, abs_partials, assert_parity, partial_ulp_check, to_host_bits,
+from gpu_helpers import (Case, TOL, abs_partials, assert_parity, partial_ulp_check, to_dev, to_host_bits,
                          to_host_values)
 
 pytestmark = pytest.mark.gpu
@@ -67,7 +67,9 @@ def test_ragged_and_small_shapes(M, N, K):
                                 dict(mma_ctas=1), dict(mma_ctas=1, unit_rows=32, grid=5),
                                 dict(mma_ctas=1, unit_rows=8, reducer_warps=1),
                                 dict(mma_ctas=2, band_m=1, unit_rows=32),
-                                dict(mma_ctas=4), dict(mma_ctas=4, grid=8, reducer_warps=2)])
+                                dict(mma_ctas=4), dict(mma_ctas=4, grid=8, reducer_warps=2),
+                                dict(adaptive=1), dict(adaptive=1, reducer_warps=6, unit_rows=8),
+                                dict(adaptive=1, mma_ctas=1, grid=5)])
 def test_plan_variants(kw):
     A, W = workloads.make_shape_inputs(520, 1000, 1024, seed=9)
     _full_check(A, W, **kw)
@@ -304,3 +306,27 @@ def test_argument_errors_on_device():
     info = p.info
     assert info.grid >= 1 and info.smem_bytes <= 232448 and info.launches[G.UNFUSED] == 2
     assert info.mma_ctas == 2 and info.tile_rows == 256 and info.grid % 2 == 0
+
+
+@pytest.mark.parametrize("op", [G.OP_RS, G.OP_AG])
+def test_tuner_picks_a_working_candidate(op):
+    """gemm_rs_tune times every candidate on the caller's buffers; the chosen
+    plan reproduces the default plan's output bit for bit."""
+    M, N, K = 1024, 2048, 2048
+    A, W = workloads.make_shape_inputs(M, N, K, seed=81, op="ag" if op == G.OP_AG else "rs")
+    Ad, Wd = to_dev(A), to_dev(W)
+    ref_plan = G.Plan(M, N, K, op=op)
+    out = torch.empty(*ref_plan.out_shape, dtype=torch.bfloat16, device="cuda")
+    ws = ref_plan.new_workspace()
+    ref_plan.run(Ad, Wd, out, ws, G.UNFUSED)
+    assert ref_plan.status() == G.GEMM_RS_OK
+    ref = out.clone()
+    best, best_us, table = G.tune(M, N, K, Ad, Wd, out, mode=G.FUSED, iters=3, rounds=3, op=op)
+    assert best_us > 0 and all(t > 0 for _, t in table)
+    assert best_us == min(t for _, t in table)
+    p = G.Plan(M, N, K, **{k: v for k, v in best.items() if k not in ("timeout_ns",)})
+    ws2 = p.new_workspace()
+    out.fill_(0)
+    p.run(Ad, Wd, out, ws2, G.FUSED)
+    assert p.status() == G.GEMM_RS_OK
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
