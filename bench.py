@@ -58,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--overlap-iters", type=int, default=200)
     p.add_argument("--chunks", type=lambda s: [int(x) for x in s.split(",") if x], default=[2, 4, 8],
                    help="chunk counts of the stream-overlap comparison (empty: skip it)")
+    p.add_argument("--sweep", default="",
+                   help="comma-separated workloads (or 'all') timed per shape instead of the "
+                        "benchmark line")
     p.add_argument("--ag-workload", default="llama3_70b_qkv_m2048",
                    help="all-gather + GEMM workload timed beside the main one ('' to skip)")
     p.add_argument("--no-allreduce", dest="allreduce", action="store_false",
@@ -156,6 +159,27 @@ class ClockSampler:
         text = open(self.path).read()
         os.unlink(self.path)
         return metrics.summarize_clocks(text)
+
+
+def time_batched(launch, iters: int, batches: int, stream) -> float:
+    """Seconds per launch: the median over `batches` of the mean of `iters`
+    back-to-back launches between two CUDA events on `stream`.  A GPU-side
+    sleep queued before each batch gives the host time to enqueue the whole
+    batch, so host launch latency never shows in the device times."""
+    import torch
+    from tensor_gemm_reduce_gb300 import metrics
+    per = []
+    for _ in range(batches):
+        torch.cuda._sleep(200_000 * iters)  # ~0.1 ms of host enqueue time per launch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            launch()
+        e1.record(stream)
+        e1.synchronize()
+        per.append(e0.elapsed_time(e1) * 1e-3 / iters)
+    return metrics.median(per)
 
 
 def blas_threads():
@@ -298,18 +322,12 @@ def run_ours(args, rank, world, local):
         b = W if b is None else b
         for _ in range(warm):
             pl.run(a, b, o, w, mode)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(iters)]
         torch.cuda.synchronize()
-        for s, e in ev:
-            s.record(stream)
-            pl.run(a, b, o, w, mode)
-            e.record(stream)
-        torch.cuda.synchronize()
+        t = time_batched(lambda: pl.run(a, b, o, w, mode), 40, max(3, iters // 40), stream)
         rc = pl.status()
         if rc != G.GEMM_RS_OK:
             raise RuntimeError(f"device status: {G.strerror(rc)}")
-        return metrics.median(s.elapsed_time(e) for s, e in ev) * 1e-3
+        return t
 
     it = args.overlap_iters
     t_gemm = time_mode(G.GEMM_ONLY, it, 20)
@@ -462,7 +480,8 @@ def run_ours(args, rank, world, local):
                     "fused_speedup_vs_best_chunked":
                         (t_chunked_best / t_fused) if t_chunked_best else None,
                     "allreduce_us": {k: v * 1e6 for k, v in t_ar.items()},
-                    "statistic": "median of per-iteration CUDA-event times, rank 0"},
+                    "statistic": "per launch: median over batches of the mean of 40 back-to-back "
+                                 "launches (queued behind a GPU sleep), rank 0"},
         "allgather_gemm": ag,
         "roofline": roof,
         "rs_roofline": rs_roof,
@@ -503,6 +522,61 @@ def run_profile_target(args, local):
     return 0
 
 
+def run_sweep(args, local):
+    """--sweep: per shape, medians of per-launch CUDA-event times of the GEMM
+    alone, the reduce alone, FUSED and UNFUSED (interleaved rounds), one JSON
+    line each.  Inputs: A ~ N(0,1), W ~ N(0,1/K) drawn on the device with a
+    seeded torch generator (the large shapes would take minutes on the host),
+    rounded to bf16 and sharded like the registered workloads; FUSED and
+    UNFUSED must agree bit for bit."""
+    import torch
+    from tensor_gemm_reduce_gb300 import gemm_rs as G
+    from tensor_gemm_reduce_gb300 import metrics, workloads
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+    names = args.sweep.split(",") if args.sweep != "all" else \
+        [w.name for w in workloads.WORKLOADS.values() if w.op == "rs" and w.name != "tiny"]
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        g = torch.Generator(device="cuda")
+        g.manual_seed(w.seed)
+        A = torch.randn(w.M, w.K, device="cuda", generator=g).bfloat16()
+        W = (torch.randn(w.K, w.N, device="cuda", generator=g) * w.K ** -0.5).bfloat16()
+        A = A.view(w.M, 8, w.K // 8).transpose(0, 1).contiguous()
+        W = W.view(8, w.K // 8, w.N).contiguous()
+        out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
+        plan = G.Plan(w.M, w.N, w.K)
+        ws = plan.new_workspace()
+        plan.run(A, W, out, ws, G.UNFUSED)
+        ref = out.clone()
+        plan.run(A, W, out, ws, G.FUSED)
+        torch.cuda.synchronize()
+        if plan.status() != G.GEMM_RS_OK or not torch.equal(ref.view(torch.int16), out.view(torch.int16)):
+            raise RuntimeError(f"{name}: fused and unfused outputs differ")
+        iters = max(5, min(40, int(20e-3 / max(w.flops / 1.5e15, 1e-6))))
+        times = {}
+        for _ in range(3):  # rounds interleave the modes: clock drift affects all alike
+            for mode, key in ((G.GEMM_ONLY, "gemm"), (G.RS_ONLY, "rs"), (G.FUSED, "fused"),
+                              (G.UNFUSED, "unfused")):
+                for _ in range(2):
+                    plan.run(A, W, out, ws, mode)
+                times.setdefault(key, []).append(
+                    time_batched(lambda: plan.run(A, W, out, ws, mode), iters, 1, stream))
+        if plan.status() != G.GEMM_RS_OK:
+            raise RuntimeError(f"{name}: device status")
+        t = {k: metrics.median(v) for k, v in times.items()}
+        print(json.dumps({
+            "sweep": name, "M": w.M, "N": w.N, "K": w.K,
+            "tflops_fused": w.flops / t["fused"] / 1e12, "tflops_gemm": w.flops / t["gemm"] / 1e12,
+            "overlap_efficiency": metrics.overlap_efficiency(t["gemm"], t["rs"], t["fused"]),
+            "fused_speedup_vs_unfused": t["unfused"] / t["fused"],
+            **{f"t_{k}_us": v * 1e6 for k, v in t.items()}, "iters": 3 * iters}), flush=True)
+        plan.close()
+        del A, W, out, ws, ref
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
@@ -510,6 +584,8 @@ def main(argv=None):
         return run_reference(args, rank, world)
     if args.profile:
         return run_profile_target(args, local)
+    if args.sweep:
+        return run_sweep(args, local)
     if world > 1:
         import torch
         import torch.distributed as dist
