@@ -364,17 +364,24 @@ class Plan:
             pass
 
 
-def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Plan] = None):
-    """One call of the row-parallel linear layer with reduce-scatter.
+def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Plan] = None,
+            **plan_kw):
+    """One call of a layer; the plan (made here from the tensors' shapes and
+    plan_kw when not given) decides which.
 
-    Returns (out, plan, workspace); out[s*M/8:(s+1)*M/8] is rank s's slice
-    (a plan made with replicas=8 gives the all-reduce: out[r] is rank r's copy).
+    Row-parallel layer (default): A [8][M][K/8], W [8][K/8][N]; out[s*M/8:(s+1)*M/8]
+    is rank s's slice (replicas=8: out[r] is rank r's copy of the whole sum).
+    All-gather + GEMM (op=OP_AG): A [8][M/8][K], W [8][K][N/8]; out[r] = C_r.
+    Returns (out, plan, workspace).
     """
     import torch
-    R, M, Kr = A.shape
-    N = W.shape[2]
     if plan is None:
-        plan = Plan(M, N, Kr * R)
+        if plan_kw.get("op", OP_RS) == OP_AG:
+            R, h, K = A.shape
+            plan = Plan(R * h, R * W.shape[2], K, **plan_kw)
+        else:
+            R, M, Kr = A.shape
+            plan = Plan(M, W.shape[2], Kr * R, **plan_kw)
     if out is None:
         out = torch.empty(*plan.out_shape, dtype=torch.bfloat16, device=A.device)
     if workspace is None:

@@ -330,3 +330,20 @@ def test_tuner_picks_a_working_candidate(op):
     p.run(Ad, Wd, out, ws2, G.FUSED)
     assert p.status() == G.GEMM_RS_OK
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_convenience_call_for_every_layer():
+    """gemm_rs() builds the plan from the tensors' shapes for each layer."""
+    A, W = workloads.make_shape_inputs(256, 512, 1024, seed=91)
+    out, plan, _ = G.gemm_rs(to_dev(A), to_dev(W))
+    ref, _ = oracle.gemm_rs(A, W)
+    assert_parity(to_host_values(out), ref, None)
+    out8, _, _ = G.gemm_rs(to_dev(A), to_dev(W), replicas=8)
+    assert tuple(out8.shape) == (8, 256, 512)
+    assert torch.equal(out8[3].view(torch.int16), out.view(torch.int16))
+    Ag, Wg = workloads.make_shape_inputs(256, 512, 1024, seed=92, op="ag")
+    c, plan, _ = G.gemm_rs(to_dev(Ag), to_dev(Wg), op=G.OP_AG)
+    assert plan.op == G.OP_AG and tuple(c.shape) == (8, 256, 64)
+    C, _ = oracle.ag_gemm(Ag, Wg)
+    got = to_host_values(c)
+    assert oracle.err_vs_oracle(got.reshape(-1, 64), C.reshape(-1, 64)) <= TOL
