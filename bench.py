@@ -61,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--sweep", default="",
                    help="comma-separated workloads (or 'all') timed per shape instead of the "
                         "benchmark line")
+    p.add_argument("--sweep-rounds", type=int, default=3)
+    p.add_argument("--sweep-iters", type=int, default=0, help="timed launches per mode and round (0: auto)")
     p.add_argument("--ag-workload", default="llama3_70b_qkv_m2048",
                    help="all-gather + GEMM workload timed beside the main one ('' to skip)")
     p.add_argument("--no-allreduce", dest="allreduce", action="store_false",
@@ -162,23 +164,23 @@ class ClockSampler:
 
 
 def time_batched(launch, iters: int, batches: int, stream) -> float:
-    """Seconds per launch: the median over `batches` of the mean of `iters`
-    back-to-back launches between two CUDA events on `stream`.  A GPU-side
-    sleep queued before each batch gives the host time to enqueue the whole
-    batch, so host launch latency never shows in the device times."""
+    """Seconds per launch: the median of iters * batches per-launch times.
+    Each batch is `iters` back-to-back launches with a CUDA event on `stream`
+    between consecutive launches; a GPU-side sleep queued before each batch
+    gives the host time to enqueue the whole batch, so host launch latency
+    never shows in the device times."""
     import torch
     from tensor_gemm_reduce_gb300 import metrics
     per = []
     for _ in range(batches):
-        torch.cuda._sleep(200_000 * iters)  # ~0.1 ms of host enqueue time per launch
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(iters):
+        torch.cuda._sleep(250_000 * iters)  # ~0.12 ms of host enqueue time per launch
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+        ev[0].record(stream)
+        for i in range(iters):
             launch()
-        e1.record(stream)
-        e1.synchronize()
-        per.append(e0.elapsed_time(e1) * 1e-3 / iters)
+            ev[i + 1].record(stream)
+        ev[-1].synchronize()
+        per.extend(ev[i].elapsed_time(ev[i + 1]) * 1e-3 for i in range(iters))
     return metrics.median(per)
 
 
@@ -480,8 +482,8 @@ def run_ours(args, rank, world, local):
                     "fused_speedup_vs_best_chunked":
                         (t_chunked_best / t_fused) if t_chunked_best else None,
                     "allreduce_us": {k: v * 1e6 for k, v in t_ar.items()},
-                    "statistic": "per launch: median over batches of the mean of 40 back-to-back "
-                                 "launches (queued behind a GPU sleep), rank 0"},
+                    "statistic": "median of 200 per-launch CUDA-event times (5 batches of 40 "
+                                 "back-to-back launches queued behind a GPU sleep), rank 0"},
         "allgather_gemm": ag,
         "roofline": roof,
         "rs_roofline": rs_roof,
@@ -553,9 +555,9 @@ def run_sweep(args, local):
         torch.cuda.synchronize()
         if plan.status() != G.GEMM_RS_OK or not torch.equal(ref.view(torch.int16), out.view(torch.int16)):
             raise RuntimeError(f"{name}: fused and unfused outputs differ")
-        iters = max(5, min(40, int(20e-3 / max(w.flops / 1.5e15, 1e-6))))
+        iters = args.sweep_iters or max(5, min(40, int(20e-3 / max(w.flops / 1.5e15, 1e-6))))
         times = {}
-        for _ in range(3):  # rounds interleave the modes: clock drift affects all alike
+        for _ in range(args.sweep_rounds):  # rounds interleave the modes: drift affects all alike
             for mode, key in ((G.GEMM_ONLY, "gemm"), (G.RS_ONLY, "rs"), (G.FUSED, "fused"),
                               (G.UNFUSED, "unfused")):
                 for _ in range(2):
@@ -570,7 +572,8 @@ def run_sweep(args, local):
             "tflops_fused": w.flops / t["fused"] / 1e12, "tflops_gemm": w.flops / t["gemm"] / 1e12,
             "overlap_efficiency": metrics.overlap_efficiency(t["gemm"], t["rs"], t["fused"]),
             "fused_speedup_vs_unfused": t["unfused"] / t["fused"],
-            **{f"t_{k}_us": v * 1e6 for k, v in t.items()}, "iters": 3 * iters}), flush=True)
+            **{f"t_{k}_us": v * 1e6 for k, v in t.items()}, "iters": args.sweep_rounds * iters}),
+            flush=True)
         plan.close()
         del A, W, out, ws, ref
         torch.cuda.empty_cache()
