@@ -184,6 +184,14 @@ def time_batched(launch, iters: int, batches: int, stream) -> float:
     return metrics.median(per)
 
 
+def device_info(index: int) -> dict:
+    import torch
+    prop = torch.cuda.get_device_properties(index)
+    return {"name": prop.name, "sms": prop.multi_processor_count,
+            "l2_mb": round(getattr(prop, "L2_cache_size", 0) / 2 ** 20, 1),
+            "hbm_gib": round(prop.total_memory / 2 ** 30, 1), "cc": f"{prop.major}.{prop.minor}"}
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -484,6 +492,7 @@ def run_ours(args, rank, world, local):
                     "allreduce_us": {k: v * 1e6 for k, v in t_ar.items()},
                     "statistic": "median of 200 per-launch CUDA-event times (5 batches of 40 "
                                  "back-to-back launches queued behind a GPU sleep), rank 0"},
+        "device": device_info(local),
         "allgather_gemm": ag,
         "roofline": roof,
         "rs_roofline": rs_roof,

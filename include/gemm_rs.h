@@ -106,7 +106,12 @@ enum gemm_rs_mode {
                                             stamps (ns, u64): start, epilogue done with its
                                             tiles, MMA issue drained, all warps done; at
                                             workspace + gemm_rs_info.trace_offset (up to
-                                            1024 CTAs) */
+                                            1024 CTAs).  The fused reduce-scatter also
+                                            stamps every reduce item when it was queued,
+                                            taken and done: u64 words 1..3 of its 32-byte
+                                            slot at workspace + gemm_rs_info.queue_offset
+                                            (word 0 holds run << 32 | item, item = 128-row
+                                            block << 5 | part) */
 
 /*
  * Problem description.  Shapes: A is [8][M][K/8] bf16 (row-major, K/8
@@ -164,6 +169,7 @@ typedef struct gemm_rs_info {
   int32_t op;             /* GEMM_RS_OP_RS or GEMM_RS_OP_AG */
   int32_t ag_direct;      /* AG: own shard read from the input, not copied */
   int64_t copy_items;     /* AG: copy items of a fused run */
+  int64_t queue_offset;   /* byte offset of the reduce-item FIFO in the workspace */
 } gemm_rs_info;
 
 /*

@@ -414,6 +414,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->chunks = h->chunks;
   info->replicas = replicas_of(&h->d);
   info->op = h->d.op;
+  info->queue_offset = (int64_t)h->lay.queue_off;
   if (h->ag) {
     info->launches[GEMM_RS_RS_ONLY] = empty || h->d.K == 0 ? 0 : 1;  // the gather kernel
     info->launches[GEMM_RS_CHUNKED] = 0;                           // not defined

@@ -228,16 +228,20 @@ __device__ __forceinline__ uint4 reduce8(const uint4 (&v)[kWorld]) {
 // acquires a slot.  One add reserves all the positions.
 __device__ __forceinline__ void queue_push_block(const GemmParams& p, int block, int parts) {
   const uint32_t pos = atomicAdd(p.ctrl + kCtrlQueueTail * kCtrlStride, (uint32_t)parts);
-  for (int sp = 0; sp < parts; ++sp)
-    st_relaxed_gpu_u64(p.queue + (size_t)(pos + sp) * kQueueStride,
-                       ((uint64_t)p.epoch << 32) | (uint32_t)((block << 5) | sp));
+  const uint64_t now = p.trace ? globaltimer_ns() : 0;
+  for (int sp = 0; sp < parts; ++sp) {
+    unsigned long long* slot = p.queue + (size_t)(pos + sp) * kQueueStride;
+    if (p.trace) st_relaxed_gpu_u64(slot + 1, now);  // debug timeline: queued
+    st_relaxed_gpu_u64(slot, ((uint64_t)p.epoch << 32) | (uint32_t)((block << 5) | sp));
+  }
 }
 
 // Take the next FIFO position and wait for its item: the item, -1 when every
 // item of the run is taken, -2 if the wait gave up.  Every lane acquires the
 // filled slot itself, so each lane's loads of the staging are ordered after
-// the releases that completed the block.
-__device__ __forceinline__ int queue_pop(const GemmParams& p, int lane) {
+// the releases that completed the block.  *slot_out: the item's FIFO slot.
+__device__ __forceinline__ int queue_pop(const GemmParams& p, int lane,
+                                         unsigned long long** slot_out) {
   uint32_t pos = 0;
   if (lane == 0) pos = atomicAdd(p.ctrl + kCtrlQueueHead * kCtrlStride, 1u);
   pos = __shfl_sync(0xffffffffu, pos, 0);
@@ -253,6 +257,7 @@ __device__ __forceinline__ int queue_pop(const GemmParams& p, int lane) {
     if (lane == 0) ready = (uint32_t)(ld_relaxed_gpu_u64(slot) >> 32) == p.epoch;
     if (__shfl_sync(0xffffffffu, ready, 0)) {
       const uint64_t v = ld_acquire_gpu_u64(slot);
+      *slot_out = const_cast<unsigned long long*>(slot);
       return (int)(uint32_t)v;
     }
     int give_up = 0;
@@ -393,7 +398,8 @@ __device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_
   Controller ctl;
   while (true) {
     if (p.adaptive && my_idx > 0 && !wait_for_share(p, my_idx, lane)) break;
-    const int item = queue_pop(p, lane);
+    unsigned long long* slot = nullptr;
+    const int item = queue_pop(p, lane, &slot);
     if (item == -1) break;
     if (item == -2) {
       if (lane == 0 && !ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride))
@@ -401,10 +407,15 @@ __device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_
       break;
     }
     const long long c0 = controller ? clock64() : 0;
+    const uint64_t t_take = (p.trace && lane == 0) ? globaltimer_ns() : 0;
     reduce_item(p, item, lane);
     __syncwarp();
     if (lane == 0) atomicAdd(cta_reduced, 1u);
     if (controller) ctl.update(p, clock64() - c0);
+    if (p.trace && lane == 0) {  // debug timeline: taken, done (words 2 and 3 of the slot)
+      st_relaxed_gpu_u64(slot + 2, t_take);
+      st_relaxed_gpu_u64(slot + 3, globaltimer_ns());
+    }
   }
 }
 

@@ -91,6 +91,7 @@ class gemm_rs_info(ctypes.Structure):
         ("op", ctypes.c_int32),
         ("ag_direct", ctypes.c_int32),
         ("copy_items", ctypes.c_int64),
+        ("queue_offset", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -351,6 +352,26 @@ class Plan:
         off = self.info.trace_offset
         n = self.info.grid * 4
         return workspace[off: off + 8 * n].view(torch.int64).view(-1, 4).cpu()
+
+    def timeline(self, workspace) -> dict:
+        """Timeline of the last FUSED reduce-scatter run of a plan made with
+        debug_flags=DEBUG_TRACE, in microseconds from the earliest CTA start:
+        per CTA (start, epilogue done, MMA drained, end) and per reduce item
+        (item, queued, taken, done).  Plain lists, ready for json.dumps."""
+        import torch
+        info = self.info
+        cta = self.trace(workspace).numpy()
+        valid = cta[:, 0] > 0
+        t0 = int(cta[valid, 0].min()) if valid.any() else 0
+        us = lambda x: [round((int(v) - t0) / 1e3, 3) if v > 0 else None for v in x]
+        q = workspace[info.queue_offset: info.queue_offset + 32 * info.units].view(torch.int64)
+        q = q.view(-1, 4).cpu().numpy()
+        items = [{"item": int(w0 & 0xFFFFFFFF), "queued": a, "taken": b, "done": c}
+                 for w0, a, b, c in zip(q[:, 0], us(q[:, 1]), us(q[:, 2]), us(q[:, 3]))]
+        return {"ctas": [{"start": a, "epilogue_done": b, "mma_drained": c, "end": d}
+                         for a, b, c, d in zip(us(cta[:, 0]), us(cta[:, 1]), us(cta[:, 2]),
+                                               us(cta[:, 3]))],
+                "items": items}
 
     def close(self):
         if getattr(self, "_h", None):

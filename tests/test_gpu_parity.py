@@ -347,3 +347,48 @@ def test_convenience_call_for_every_layer():
     C, _ = oracle.ag_gemm(Ag, Wg)
     got = to_host_values(c)
     assert oracle.err_vs_oracle(got.reshape(-1, 64), C.reshape(-1, 64)) <= TOL
+
+
+def test_debug_timeline_is_consistent():
+    """DEBUG_TRACE: every reduce item is queued, then taken, then done, within
+    the CTAs' lifetime; the output is the normal one."""
+    A, W = workloads.make_shape_inputs(1024, 2048, 2048, seed=93)
+    c = Case(A, W, debug_flags=G.DEBUG_TRACE)
+    out = c.run(G.FUSED, poison=True)
+    tl = c.plan.timeline(c.ws)
+    items = tl["items"]
+    assert len(items) == c.plan.info.units
+    assert sorted(it["item"] for it in items) == sorted(set(it["item"] for it in items))
+    end = max(x["end"] for x in tl["ctas"] if x["end"] is not None)
+    for it in items:
+        assert it["queued"] is not None and it["taken"] is not None and it["done"] is not None
+        assert 0 <= it["queued"] <= it["taken"] + 2.1 and it["taken"] <= it["done"] <= end + 2.1
+    ref = Case(A, W).run(G.FUSED)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("layer", ["rs", "allreduce", "ag"])
+def test_guard_bands_untouched(layer):
+    """Canary bands around the output and after the workspace, and the inputs,
+    are left as they were by every mode (no write out of bounds)."""
+    M, N, K = 392, 1536, 1600
+    op = G.OP_AG if layer == "ag" else G.OP_RS
+    A, W = workloads.make_shape_inputs(M, N, K, seed=94, op="ag" if layer == "ag" else "rs")
+    plan = G.Plan(M, N, K, op=op, replicas=8 if layer == "allreduce" else 0)
+    guard = 4096
+    n_out = int(np.prod(plan.out_shape))
+    big_out = torch.full((guard + n_out + guard,), -7, dtype=torch.int16, device="cuda")
+    out = big_out[guard:guard + n_out].view(torch.bfloat16).view(*plan.out_shape)
+    big_ws = torch.full((plan.workspace_bytes + guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = big_ws[:plan.workspace_bytes]
+    Ad, Wd = to_dev(A), to_dev(W)
+    A0, W0 = Ad.clone(), Wd.clone()
+    modes = [G.FUSED, G.UNFUSED, G.GEMM_ONLY, G.RS_ONLY] + ([G.CHUNKED] if op == G.OP_RS else [])
+    for mode in modes:
+        plan.run(Ad, Wd, out, ws, mode)
+        assert plan.status() == G.GEMM_RS_OK
+        torch.cuda.synchronize()
+        assert torch.all(big_out[:guard] == -7) and torch.all(big_out[guard + n_out:] == -7), mode
+        assert torch.all(big_ws[plan.workspace_bytes:] == 0x5A), mode
+        assert torch.equal(Ad.view(torch.int16), A0.view(torch.int16)) and torch.equal(
+            Wd.view(torch.int16), W0.view(torch.int16)), mode
