@@ -59,8 +59,9 @@ def parse_args(argv=None):
     p.add_argument("--chunks", type=lambda s: [int(x) for x in s.split(",") if x], default=[2, 4, 8],
                    help="chunk counts of the stream-overlap comparison (empty: skip it)")
     p.add_argument("--sweep", default="",
-                   help="comma-separated workloads (or 'all') timed per shape instead of the "
-                        "benchmark line")
+                   help="comma-separated workloads ('all': every reduce-scatter shape, 'all_ag': every "
+                        "all-gather shape) timed per shape instead of the benchmark line; for "
+                        "all-gather shapes t_rs is the gather alone")
     p.add_argument("--sweep-rounds", type=int, default=3)
     p.add_argument("--sweep-iters", type=int, default=0, help="timed launches per mode and round (0: auto)")
     p.add_argument("--ag-workload", default="llama3_70b_qkv_m2048",
@@ -545,18 +546,26 @@ def run_sweep(args, local):
     from tensor_gemm_reduce_gb300 import metrics, workloads
     torch.cuda.set_device(local)
     stream = torch.cuda.current_stream()
-    names = args.sweep.split(",") if args.sweep != "all" else \
-        [w.name for w in workloads.WORKLOADS.values() if w.op == "rs" and w.name != "tiny"]
+    if args.sweep == "all":
+        names = [w.name for w in workloads.WORKLOADS.values() if w.op == "rs" and w.name != "tiny"]
+    elif args.sweep == "all_ag":
+        names = [w.name for w in workloads.WORKLOADS.values() if w.op == "ag" and w.name != "tiny_ag"]
+    else:
+        names = args.sweep.split(",")
     for name in names:
         w = workloads.WORKLOADS[name]
         g = torch.Generator(device="cuda")
         g.manual_seed(w.seed)
         A = torch.randn(w.M, w.K, device="cuda", generator=g).bfloat16()
         W = (torch.randn(w.K, w.N, device="cuda", generator=g) * w.K ** -0.5).bfloat16()
-        A = A.view(w.M, 8, w.K // 8).transpose(0, 1).contiguous()
-        W = W.view(8, w.K // 8, w.N).contiguous()
-        out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
-        plan = G.Plan(w.M, w.N, w.K)
+        if w.op == "ag":  # row shards of A, column shards of W (all-gather + GEMM)
+            A = A.view(8, w.M // 8, w.K).contiguous()
+            W = W.view(w.K, 8, w.N // 8).transpose(0, 1).contiguous()
+        else:
+            A = A.view(w.M, 8, w.K // 8).transpose(0, 1).contiguous()
+            W = W.view(8, w.K // 8, w.N).contiguous()
+        plan = G.Plan(w.M, w.N, w.K, op=G.OP_AG if w.op == "ag" else G.OP_RS)
+        out = torch.empty(*plan.out_shape, dtype=torch.bfloat16, device="cuda")
         ws = plan.new_workspace()
         plan.run(A, W, out, ws, G.UNFUSED)
         ref = out.clone()
@@ -577,7 +586,8 @@ def run_sweep(args, local):
             raise RuntimeError(f"{name}: device status")
         t = {k: metrics.median(v) for k, v in times.items()}
         print(json.dumps({
-            "sweep": name, "M": w.M, "N": w.N, "K": w.K,
+            "sweep": name, "layer": "all-gather + GEMM" if w.op == "ag" else "GEMM + reduce-scatter",
+            "M": w.M, "N": w.N, "K": w.K,
             "tflops_fused": w.flops / t["fused"] / 1e12, "tflops_gemm": w.flops / t["gemm"] / 1e12,
             "overlap_efficiency": metrics.overlap_efficiency(t["gemm"], t["rs"], t["fused"]),
             "fused_speedup_vs_unfused": t["unfused"] / t["fused"],

@@ -134,7 +134,8 @@ def test_unpublished_copy_times_out_and_recovers():
     bad.run(G.UNFUSED)  # the debug plan itself is usable again
 
 
-@pytest.mark.parametrize("name", ["llama3_70b_qkv_m2048"])
+@pytest.mark.parametrize("name", ["llama3_70b_qkv_m2048",
+                                  pytest.param("flux_fig4_ag_m1024", marks=pytest.mark.slow)])
 def test_workload_sampled(name):
     w = workloads.WORKLOADS[name]
     A, W = workloads.make_inputs(w)
