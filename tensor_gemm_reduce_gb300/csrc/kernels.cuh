@@ -1,4 +1,6 @@
-// kernels.cuh -- the device side of the fused GEMM + reduce-scatter.
+// kernels.cuh -- the device side: the fused GEMM + reduce-scatter (also
+// all-reduce), the fused all-gather + GEMM, and the standalone kernels of the
+// unfused paths.
 //
 // Problem page "A fused GEMM + reduce-scatter kernel hiding 90% of
 // communication on 8 H100 GPUs": "What is asked" (partials summed across the
@@ -27,10 +29,15 @@
 //                 add on the 128-row block's completion count; the add that
 //                 completes a block (the last of 8 ranks x 4 warps) appends the
 //                 block's reduce items to a global FIFO
-//   warps 6..     reducers (fused kernel only): take the next FIFO position,
-//                 wait (acquire) until its item is there, add the 8 bf16
-//                 partials in fp32 in rank order, write bf16 output.  The
-//                 epilogue warps join them when the CTA's tiles are done.
+//   warps 6..     reducers (fused reduce-scatter): take the next FIFO
+//                 position, wait (acquire) until its item is there, add the 8
+//                 bf16 partials in fp32 in rank order, write bf16 output (to
+//                 every rank's copy for the all-reduce).  The epilogue warps
+//                 join them when the CTA's tiles are done; optionally a
+//                 controller sets how many of them take items (adaptive share).
+//                 In the fused all-gather the same warps are copy warps that
+//                 gather A's row shards into each rank's buffer, and the
+//                 producer waits for a shard's copies before loading its rows.
 // Every wait is bounded by p.timeout_ns; on expiry the kernel records an error
 // word, stops its loops, lets its in-flight copies land, frees TMEM and returns.
 #pragma once
