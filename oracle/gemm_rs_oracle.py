@@ -175,8 +175,10 @@ def slices(out: np.ndarray, world: int = WORLD):
 
 
 # ---------------------------------------------------------------------------
-# The correctness rule ("How it gets verified": BF16 tolerance, max relative
-# error at most 1.1x the unfused path against an FP32 reference)
+# The correctness rule (problem page, section "How it gets verified"): the
+# output is accepted when it is within bf16 accuracy and its largest relative
+# error against a high-precision reference is no more than 1.1 times the
+# unfused path's
 # ---------------------------------------------------------------------------
 
 

@@ -6,9 +6,9 @@ them once to bf16 (through torch's float32 -> bfloat16 conversion, which rounds
 to nearest even) and lays them out as per-rank shards.
 
 Shapes follow the problem page "A fused GEMM + reduce-scatter kernel hiding 90%
-of communication on 8 H100 GPUs" (section "How it gets verified": tokens M in
-{512, 2048, 8192, 32768}, (N, K) from the Llama-3 70B and Mixtral 8x22B
-projections, TP degree 8).  Row-parallel sharding follows the FLUX page,
+of communication on 8 H100 GPUs" (section "How it gets verified": token counts
+M of 512, 2048, 8192 and 32768, output and inner dimensions of Llama-3-70B and
+Mixtral-8x22B projection layers, 8-way tensor parallelism).  Row-parallel sharding follows the FLUX page,
 Figure 2 (N-way partition of the MLP forward, batch and sequence flattened
 into the GEMM's M): rank r holds columns [r*K/8, (r+1)*K/8) of A and the
 matching rows of W.

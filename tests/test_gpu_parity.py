@@ -1,9 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
 Correctness rule (problem page "A fused GEMM + reduce-scatter kernel hiding
-90% of communication on 8 H100 GPUs", section "How it gets verified"): output
-within bf16 tolerance, max relative error at most 1.1x the unfused path's
-against an FP32 (here float64) reference.  The threshold on the oracle is
+90% of communication on 8 H100 GPUs", section "How it gets verified"): the
+output must be as accurate as bf16 allows, and its largest relative error
+against a high-precision reference (here float64) may exceed the unfused
+path's by at most a factor 1.1.  The threshold on the oracle is
 max|X - oracle| / max|oracle| <= 1e-2.  Beyond the rule, the fused and the
 unfused paths are required to agree bit for bit (same tile code, same
 rank-order fp32 sum), and the per-rank bf16 partials are checked against the

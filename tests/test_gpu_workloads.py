@@ -4,9 +4,9 @@ fused and unfused outputs bit for bit, the per-rank partials of the sampled
 rows, and whole-output properties (finite, slice statistics).
 
 Workloads: problem page "A fused GEMM + reduce-scatter kernel hiding 90% of
-communication on 8 H100 GPUs", section "How it gets verified" (M in {512,
-2048, 8192, 32768}, (N, K) from the Llama-3 70B and Mixtral 8x22B
-projections, TP degree 8).
+communication on 8 H100 GPUs", section "How it gets verified": token counts
+M of 512 to 32768 and the output and inner dimensions of Llama-3-70B and
+Mixtral-8x22B projection layers, 8-way tensor parallelism.
 """
 import numpy as np
 import pytest
