@@ -15,7 +15,7 @@ verified"; FLUX page, Figure 2):
   are summed across ranks and each rank keeps one row slice of the total: rank
   s receives rows [s*M/8, (s+1)*M/8) (a reduce-scatter).
 
-Readings of points the pages leave open (each one is listed in the design doc):
+Readings of points the pages leave open:
   * each partial is rounded to bf16 once, round to nearest even, directly from
     its exact value (the bf16 tensor a real reduce-scatter would move);
   * the sum over ranks is a left fold in FP32 (IEEE, round to nearest even),
