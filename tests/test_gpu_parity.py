@@ -62,7 +62,7 @@ def test_ragged_and_small_shapes(M, N, K):
 
 
 @pytest.mark.parametrize("kw", [dict(reducer_warps=1), dict(reducer_warps=6), dict(grid=3),
-                                dict(band_m=1), dict(unit_rows=8), dict(unit_rows=32),
+                                dict(band_m=1), dict(unit_rows=8), dict(unit_rows=16), dict(unit_rows=32),
                                 dict(grid=1, reducer_warps=2),
                                 dict(debug_flags=G.DEBUG_NO_STAGING_L2),
                                 dict(mma_ctas=1), dict(mma_ctas=1, unit_rows=32, grid=5),
