@@ -126,7 +126,7 @@ typedef struct gemm_rs_desc {
                              0 = default (4; all-gather 2) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
-  int32_t unit_rows;      /* rows per reduce item in FUSED mode: 4, 8, 16 or 32; 0 = 4 */
+  int32_t unit_rows;      /* rows per reduce item in FUSED mode: 4, 8, 16 or 32; 0 = 8 */
   uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
   uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
   int32_t mma_ctas;       /* CTAs of a cluster sharing one tile: 1 (128 x 256 tiles), 2 (a
@@ -142,6 +142,10 @@ typedef struct gemm_rs_desc {
   int32_t adaptive;       /* FUSED reduce-scatter: 1 = an on-GPU controller sets how many of
                              each CTA's reducer warps take items, from cycle and progress
                              counters (mKernel page, section 3.2); 0 = all of them */
+  int32_t tail_waves;     /* FUSED reduce-scatter: regions completed by the last tail_waves
+                             waves of tiles are reduced in 4-row items (fine grain where the
+                             reduction is the critical path), the others in unit_rows-row
+                             items; 0 = default (3), 1..64 */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -281,7 +285,7 @@ int gemm_rs_destroy(gemm_rs_t plan);
  * section 5.5: the best share of communication workers varies with the kernel
  * and the shape).  The candidates for d's problem are d with, in turn:
  *   reduce-scatter / all-reduce: mma_ctas in {2, 1} x reducer_warps in {2, 4, 6}
- *     x unit_rows in {4, 8};
+ *     x unit_rows in {8, 16};
  *   all-gather: mma_ctas in {2, 1} x copy warps (reducer_warps) in {1, 2, 4};
  * every other field as in d.  gemm_rs_tune_candidates writes up to `max` of them
  * to `cands` (may be NULL), sets *count, and *workspace_bytes (may be NULL) to

@@ -20,10 +20,14 @@ namespace {
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultReducerWarps = 4;
 constexpr int kDefaultCopyWarps = 2;
-// rows per reduce item: small items finish in one round of loads, so less
-// reduction is in flight when the last tiles finish (4 rows: o_proj fused
-// 209 -> 204 us, M = 512 76 -> 70 us against 16 rows)
-constexpr int kDefaultUnitRows = 4;
+// Reduce item size: small items leave less reduction in service when the
+// last tiles finish, large ones cost fewer FIFO operations where the
+// reduction is a large share of the work.  8-row items, and 4-row items for
+// the regions of the last 3 waves, were the best compromise measured (o_proj
+// fused 211 -> 206 us, M = 512 78 -> 72 us against 16-row items and a
+// 1-wave tail; 8192^3 at most 3% slower).
+constexpr int kDefaultUnitRows = 8;
+constexpr int kDefaultTailWaves = 3;
 constexpr int kDefaultMmaCtas = 2;
 constexpr int kDefaultChunks = 4;
 constexpr int kMaxChunks = 64;
@@ -76,6 +80,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->replicas != 0 && d->replicas != 1 && d->replicas != kWorld) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op != GEMM_RS_OP_RS && d->op != GEMM_RS_OP_AG) return GEMM_RS_ERR_INVALID_ARG;
   if (d->adaptive != 0 && d->adaptive != 1) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->tail_waves < 0 || d->tail_waves > 64) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op == GEMM_RS_OP_AG && d->replicas > 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
@@ -126,10 +131,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int mma_ctas_of(const gemm_rs_desc* d) { return d->mma_ctas > 0 ? d->mma_ctas : kDefaultMmaCtas; }
 int replicas_of(const gemm_rs_desc* d) { return d->replicas > 1 ? d->replicas : 1; }
 
-// First region completed by the last wave of tiles (tiles are claimed in
-// order, `lanes` at a time; a region's 8 rank tiles are consecutive).
-long long tail_region_of(long long tiles, long long lanes, long long regions) {
-  long long first_last_wave_tile = tiles - lanes;
+// First region completed by the last `waves` waves of tiles (tiles are
+// claimed in order, `lanes` at a time; a region's 8 rank tiles are
+// consecutive).
+long long tail_region_of(long long tiles, long long lanes, long long regions, int waves) {
+  long long first_last_wave_tile = tiles - lanes * waves;
   if (first_last_wave_tile < 0) first_last_wave_tile = 0;
   long long r = first_last_wave_tile / kWorld;
   return r < regions ? r : regions;
@@ -355,7 +361,8 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   h->splits = kBM / h->unit_rows;
   h->blocks_per_region = h->tile_rows / kBM;
   const long long blocks = (long long)h->mt * h->nt * h->blocks_per_region;
-  h->tail_region = tail_region_of(h->tiles, h->grid / pair, (long long)h->mt * h->nt);
+  h->tail_region = tail_region_of(h->tiles, h->grid / pair, (long long)h->mt * h->nt,
+                                  d->tail_waves > 0 ? d->tail_waves : kDefaultTailWaves);
   h->items = items_of(blocks, h->blocks_per_region, h->tail_region, h->splits);
   h->lay = layout_for(d->M, d->N, blocks, h->items);
   {  // CHUNKED: whole tile rows per chunk
@@ -439,7 +446,7 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
   const bool ag = d->op == GEMM_RS_OP_AG;
   static const int kCtas[2] = {2, 1};
   static const int kWarpsRs[3] = {2, 4, 6}, kWarpsAg[3] = {1, 2, 4};
-  static const int kUnits[2] = {4, 8};
+  static const int kUnits[2] = {8, 16};
   int n = 0;
   size_t ws_max = 0;
   for (int c = 0; c < 2; ++c)
@@ -1077,7 +1084,8 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.blocks_per_region = tile_rows / kBM;
     p.tile_rows = tile_rows;
     p.num_tiles = (long long)kWorld * mt * nt;
-    const long long tail = tail_region_of(p.num_tiles, nd->grid / kDefaultMmaCtas, mt * nt);
+    const long long tail =
+        tail_region_of(p.num_tiles, nd->grid / kDefaultMmaCtas, mt * nt, kDefaultTailWaves);
     p.tail_region = (int)tail;
     p.num_items = items_of(blocks, p.blocks_per_region, tail, p.splits);
     p.flag_target = (uint32_t)(kWorld * kEpiWarps);  // counts were just cleared: one run's adds

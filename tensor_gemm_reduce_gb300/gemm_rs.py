@@ -64,6 +64,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("replicas", ctypes.c_int32),
         ("op", ctypes.c_int32),
         ("adaptive", ctypes.c_int32),
+        ("tail_waves", ctypes.c_int32),
     ]
 
 
@@ -176,9 +177,9 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, adaptive=0, world=WORLD):
+          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, adaptive=0, tail_waves=0, world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas, chunks, replicas, op, adaptive)
+                        debug_flags, mma_ctas, chunks, replicas, op, adaptive, tail_waves)
 
 
 # ----------------------------------------------------------------------------
@@ -257,12 +258,13 @@ class Plan:
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
                  mma_ctas: int = 0, chunks: int = 0, replicas: int = 0, op: int = OP_RS,
-                 adaptive: int = 0):
+                 adaptive: int = 0, tail_waves: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.replicas = max(1, int(replicas))
         self.op = int(op)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
-                          timeout_ns, debug_flags, mma_ctas, chunks, replicas, op, adaptive)
+                          timeout_ns, debug_flags, mma_ctas, chunks, replicas, op, adaptive,
+                          tail_waves)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property
@@ -417,7 +419,7 @@ def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Pl
 
 TUNE_MAX = 16
 _DESC_KW = ("reducer_warps", "grid", "band_m", "unit_rows", "timeout_ns", "debug_flags",
-            "mma_ctas", "chunks", "replicas", "op", "adaptive")
+            "mma_ctas", "chunks", "replicas", "op", "adaptive", "tail_waves")
 
 
 def tune_candidates(desc: gemm_rs_desc):

@@ -44,6 +44,8 @@ def _create(**kw):
     (dict(chunks=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(chunks=65), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(replicas=2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(tail_waves=65), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(tail_waves=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=G.OP_AG, replicas=8), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=G.OP_AG, N=264), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),

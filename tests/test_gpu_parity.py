@@ -70,7 +70,8 @@ def test_ragged_and_small_shapes(M, N, K):
                                 dict(mma_ctas=2, band_m=1, unit_rows=32),
                                 dict(mma_ctas=4), dict(mma_ctas=4, grid=8, reducer_warps=2),
                                 dict(adaptive=1), dict(adaptive=1, reducer_warps=6, unit_rows=8),
-                                dict(adaptive=1, mma_ctas=1, grid=5)])
+                                dict(adaptive=1, mma_ctas=1, grid=5),
+                                dict(unit_rows=4, tail_waves=1), dict(unit_rows=16, tail_waves=64)])
 def test_plan_variants(kw):
     A, W = workloads.make_shape_inputs(520, 1000, 1024, seed=9)
     _full_check(A, W, **kw)
