@@ -162,3 +162,17 @@ def test_tune_candidates_and_their_workspace(lib, op):
     assert ws > staging
     with pytest.raises(G.GemmRSError):
         G.tune_candidates(G._desc(100, 256, 512))
+
+
+def test_header_is_plain_c():
+    """include/gemm_rs.h compiles as strict C99 (no C++ in the boundary)."""
+    import os
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-fsyntax-only", "-x", "c",
+                        os.path.join(root, "include", "gemm_rs.h")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -394,3 +394,28 @@ def test_guard_bands_untouched(layer):
         assert torch.all(big_ws[plan.workspace_bytes:] == 0x5A), mode
         assert torch.equal(Ad.view(torch.int16), A0.view(torch.int16)) and torch.equal(
             Wd.view(torch.int16), W0.view(torch.int16)), mode
+
+
+def test_pure_c_caller(tmp_path):
+    """The C ABI used from a C program (no Python, no PyTorch): an exact-integer
+    fused run through gemm_rs_run_host, checked on the host in C."""
+    import os
+    import shutil
+    import subprocess
+    from tensor_gemm_reduce_gb300 import build as B
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib_dir = os.path.dirname(B.LIB)
+    cuda_home = os.path.dirname(os.path.dirname(B.nvcc_path()))
+    exe = str(tmp_path / "abi_smoke")
+    r = subprocess.run([cc, "-std=c99", "-O1", os.path.join(root, "tests", "c_abi", "abi_smoke.c"),
+                        "-I" + os.path.join(root, "include"), "-I" + os.path.join(cuda_home, "include"),
+                        "-L" + lib_dir, "-Wl,-rpath," + lib_dir, "-lgemm_rs",
+                        "-L" + os.path.join(cuda_home, "lib64"), "-Wl,-rpath," + os.path.join(cuda_home, "lib64"),
+                        "-lcudart", "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "exact" in r.stdout
