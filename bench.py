@@ -75,7 +75,8 @@ def parse_args(argv=None):
                    help="target length of the whole --impl reference run")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile", choices=["fused", "unfused", "gemm_only", "rs_only"], default=None,
-                   help="only run --warmup + --steps launches of one mode (a target for ncu)")
+                   help="only run --warmup + --steps launches of one mode of --workload (a target "
+                        "for ncu; for an all-gather workload rs_only is the gather alone)")
     return p.parse_args(argv)
 
 
@@ -519,12 +520,15 @@ def run_profile_target(args, local):
     A_bits, W_bits = workloads.make_inputs(w)
     A = torch.from_numpy(A_bits.view(np.int16)).cuda().view(torch.bfloat16)
     W = torch.from_numpy(W_bits.view(np.int16)).cuda().view(torch.bfloat16)
-    out = torch.empty(w.M, w.N, dtype=torch.bfloat16, device="cuda")
-    plan = G.Plan(w.M, w.N, w.K)
+    op = G.OP_AG if w.op == "ag" else G.OP_RS
+    plan = G.Plan(w.M, w.N, w.K, op=op)
+    out = torch.empty(*plan.out_shape, dtype=torch.bfloat16, device="cuda")
     ws = plan.new_workspace()
     mode = G.MODES[args.profile]
-    if mode == G.RS_ONLY:
-        plan.run(A, W, out, ws, G.GEMM_ONLY)
+    if mode == G.RS_ONLY and op == G.OP_RS:
+        plan.run(A, W, out, ws, G.GEMM_ONLY)  # partials in the staging for the reduce alone
+    if mode == G.GEMM_ONLY and op == G.OP_AG:
+        plan.run(A, W, out, ws, G.RS_ONLY)  # gathered buffers for the GEMM alone
     for _ in range(args.warmup + args.steps):
         plan.run(A, W, out, ws, mode)
     rc = plan.status()

@@ -752,6 +752,11 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
   p.ag_order = 1;
   p.copy_items = h->copy_items;
   p.copy_chunk = kCopyChunk;
+  // pace the copies when one rank's tiles take at least two waves: then a
+  // rank's gathered buffer written one rank ahead is still in L2 when read
+  // (FLUX Figure 4 all-gather, M = 2048: 1597 -> 1521 us); shorter ranks
+  // leave too little slack for it (QKV 2048 x 10240 x 8192: 251 -> 254 us)
+  p.copy_paced = (long long)h->mt * h->nt >= 2LL * (h->grid / h->pair);
   if (fused) {
     h->epoch += 1;
     p.ag_target = (uint32_t)h->chunks_per_shard * h->epoch;  // every copied (rank, shard)

@@ -131,6 +131,7 @@ struct GemmParams {
   int ag_order;            // tiles in the all-gather order (ag_tile_at), also when unfused
   long long copy_items;    // copy items of a run
   long long copy_chunk;    // elements per copy item
+  int copy_paced;          // copy rank r's shards only once rank r - 1's tiles are claimed
   uint16_t* stage;   // rank r's partial of output element (i, j): stage[r * plane + i * N + j]
   long long plane;   // elements from one rank's staging region to the next
   uint16_t* out;
@@ -483,6 +484,21 @@ __device__ __noinline__ void copy_loop(const GemmParams& p, int lane) {
     i = __shfl_sync(0xffffffffu, i, 0);
     if ((long long)i >= p.copy_items) break;
     const int r = (int)(i / per_rank);
+    if (p.copy_paced && r > 1) {
+      // Paced copies: rank r's shards are written only once the GEMM has begun
+      // claiming rank r - 1's tiles, so they are still in L2 when rank r's
+      // tiles read them (copied all at once, the 8 buffers outgrow L2 and are
+      // read back from DRAM).  Bounded; a late copy only delays its tiles.
+      if (lane == 0) {
+        const long long need = (long long)(r - 1) * p.mt_count * p.nt_count;
+        const uint64_t t0 = globaltimer_ns();
+        while ((long long)ld_volatile_u32(p.ctrl + kCtrlTileTicket * kCtrlStride) < need &&
+               !ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride) &&
+               globaltimer_ns() - t0 < p.timeout_ns)
+          __nanosleep(500);
+      }
+      __syncwarp();
+    }
     const long long rem = i % per_rank;
     const int k = (int)(rem / p.chunks_per_shard) + p.first_round;
     const long long c = rem % p.chunks_per_shard;

@@ -92,6 +92,8 @@ def test_tiny_workload():
     (1024, 1536, 2048, dict(mma_ctas=4), False),   # 512-row tiles over 128-row shards
     (2048, 2560, 1024, dict(reducer_warps=1, grid=6), True),  # one copy warp, few CTAs
     (2048, 2560, 1024, dict(reducer_warps=6), True),
+    (2048, 4096, 512, dict(grid=8), True),   # 16 tiles per rank >= 2 waves of 4 clusters: paced copies
+    (1024, 4096, 512, dict(grid=4, mma_ctas=1), True),  # paced, 1-CTA tiles
 ])
 def test_shapes_and_plans(M, N, K, kw, direct):
     A, W = workloads.make_shape_inputs(M, N, K, seed=M + 2 * N + K, op="ag")
