@@ -200,8 +200,9 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
  * Returns after enqueueing; device-side failures (timeouts) are reported by
  * gemm_rs_status.  CHUNKED also uses a second stream and events that the plan
  * creates on its first CHUNKED call; that stream joins `stream` again before
- * the call returns (work after it on `stream` sees the whole output).  Modes that do not read A/W (RS_ONLY) or write out
- * (GEMM_ONLY) accept NULL for them.
+ * the call returns (work after it on `stream` sees the whole output).  Modes
+ * that do not read A/W (RS_ONLY) or write out (GEMM_ONLY) accept NULL for
+ * them.
  */
 int gemm_rs_run(gemm_rs_t plan, int mode, const void* A, const void* W,
                 void* out, void* workspace, void* stream);
@@ -211,9 +212,11 @@ int gemm_rs_run(gemm_rs_t plan, int mode, const void* A, const void* W,
  * host memory.  Enqueued on `stream`, in this order: copy A_host -> A_dev
  * (8*M*(K/8)*2 bytes) and W_host -> W_dev (8*(K/8)*N*2 bytes), run `mode`
  * exactly as gemm_rs_run would on the device buffers, copy out_dev -> out_host
- * (replicas*M*N*2 bytes).  All six buffers belong to the caller; host buffers should be
- * pinned (cudaHostAlloc / cudaHostRegister) for the copies to be asynchronous,
- * and must stay valid until the stream has passed the copies.  RS_ONLY copies
+ * (replicas*M*N*2 bytes).  All six buffers belong to the caller; host buffers
+ * should be pinned (cudaHostAlloc / cudaHostRegister) for the copies to be
+ * asynchronous, and must stay valid until the stream has passed the copies.
+ * Two plans with their own device buffers, on two streams, let one call's
+ * copies overlap the other's kernel.  RS_ONLY copies
  * nothing in, GEMM_ONLY copies nothing out.  Same return codes as gemm_rs_run,
  * plus GEMM_RS_ERR_CUDA if a copy cannot be enqueued.
  */
@@ -225,9 +228,9 @@ int gemm_rs_run_host(gemm_rs_t plan, int mode, const void* A_host, const void* W
  * Synchronise `stream` and report the device error word of the workspace the
  * plan used last: GEMM_RS_OK, GEMM_RS_ERR_TIMEOUT (a device wait gave up; the
  * output of that run is incomplete), GEMM_RS_ERR_INCOMPLETE (the run ended
- * with output blocks that never received all 8 partials) or GEMM_RS_ERR_CUDA.  A non-OK result
- * also clears the workspace's control words and flags so the next run starts
- * clean.
+ * with output blocks that never received all 8 partials) or GEMM_RS_ERR_CUDA.
+ * A non-OK result also clears the workspace's control words and flags so the
+ * next run starts clean.
  */
 int gemm_rs_status(gemm_rs_t plan, void* stream);
 
