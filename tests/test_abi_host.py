@@ -25,6 +25,21 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(G._SIGS), "binding signatures and header out of sync"
 
 
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library the binding raises; nothing computes on the CPU."""
+    from tensor_gemm_reduce_gb300 import build
+    monkeypatch.setattr(G, "_LIB", None)
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "libgemm_rs.so"))
+    with pytest.raises(ImportError):
+        G.load_library(build_if_missing=False)
+    # a plan needs the library; when it cannot be built the call raises
+    def no_compiler():
+        raise RuntimeError("nvcc not found")
+    monkeypatch.setattr(build, "build_library", no_compiler)
+    with pytest.raises(RuntimeError, match="nvcc not found"):
+        G.Plan(64, 256, 512)
+
+
 def _create(**kw):
     d = G._desc(kw.pop("M", 128), kw.pop("N", 256), kw.pop("K", 512), **kw)
     h = ctypes.c_void_p()
