@@ -17,7 +17,9 @@ verified"; FLUX page, Figure 2):
 
 Readings of points the pages leave open:
   * each partial is rounded to bf16 once, round to nearest even, directly from
-    its exact value (the bf16 tensor a real reduce-scatter would move);
+    its exact value (the bf16 tensor a real reduce-scatter would move): a
+    float64 matmul, with the elements whose float64 error could change that
+    rounding summed exactly (bf16_of_exact_product);
   * the sum over ranks is a left fold in FP32 (IEEE, round to nearest even),
     starting from the rank-0 partial and adding ranks 1..7 in order;
   * the FP32 total is rounded to bf16, round to nearest even;
@@ -36,6 +38,8 @@ tests/test_oracle_pins.py (exact rational brute force, closed forms, invariants
 and library routines).
 """
 from __future__ import annotations
+
+from fractions import Fraction
 
 import numpy as np
 
@@ -64,6 +68,57 @@ def bf16_round(x) -> np.ndarray:
     return np.where(np.isfinite(x), y, x)
 
 
+def bf16_round_fraction(x: Fraction) -> float:
+    """Round an exact rational to the nearest bf16 value, ties to even
+    (8 significant bits, quantum never below 2**-133, inf from 2**128 up)."""
+    if x == 0:
+        return 0.0
+    sign = -1.0 if x < 0 else 1.0
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()  # 2**(e-1) < a < 2**(e+1)
+    if a >= Fraction(2) ** e:
+        e += 1                                                  # now 2**(e-1) <= a < 2**e
+    qe = max(e - 8, -133)
+    n = a / Fraction(2) ** qe
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    v = Fraction(fl) * Fraction(2) ** qe
+    return sign * (float("inf") if v >= Fraction(2) ** 128 else float(v))
+
+
+def bf16_of_exact_product(X, Y, S=None) -> np.ndarray:
+    """bf16(X @ Y) rounded once from the exact value, for bf16 X [M][k] and
+    Y [k][N] (values).
+
+    S = X @ Y in float64 (computed here unless given): every product of two
+    bf16 values is exact in float64 and only the k - 1 additions round, by at
+    most k * 2**-53 * sum|x||y| whatever the summation order.  Where the
+    interval S +- e (e = 4 times that bound, covering the interval's own
+    rounding) rounds to one bf16 value, the exact value inside it rounds to
+    the same value (rounding is monotone).  At the other elements the exact
+    value could lie across a bf16 midpoint from S (products of very different
+    magnitudes); those are summed exactly with fractions and rounded.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    Y = np.asarray(Y, dtype=np.float64)
+    if S is None:
+        S = X @ Y
+    Q = bf16_round(S)
+    k = X.shape[1]
+    if k <= 1 or Q.size == 0:
+        return Q  # one product (or none): S is exact
+    e = 4.0 * k * 2.0 ** -53 * (np.abs(X) @ np.abs(Y))
+    with np.errstate(invalid="ignore", over="ignore"):
+        unsure = (bf16_round(S - e) != bf16_round(S + e)) & np.isfinite(S) & np.isfinite(e)
+    for i, j in zip(*np.nonzero(unsure)):
+        exact = sum((Fraction(float(X[i, t])) * Fraction(float(Y[t, j])) for t in range(k)),
+                    Fraction(0))
+        Q[i, j] = bf16_round_fraction(exact)
+    return Q
+
+
 def bf16_from_bits(bits) -> np.ndarray:
     """uint16 bf16 bit patterns -> float64 values (exact)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
@@ -82,11 +137,12 @@ def bf16_to_bits(values) -> np.ndarray:
 
 
 def rank_partials(A_shards, W_shards) -> np.ndarray:
-    """Exact per-rank partial products S_r = A_r @ W_r in float64.
+    """Per-rank partial products S_r = A_r @ W_r in float64.
 
     A_shards: [8][M][Kr] (bf16 bits or float values), W_shards: [8][Kr][N].
     Inputs are bf16, so every product is exact in float64 and the float64
-    matmul only rounds its running sums (relative error ~ Kr * 2**-53).
+    matmul only rounds its running sums (relative error ~ Kr * 2**-53); see
+    partials_bf16 for the partials' exactly rounded bf16 values.
     """
     A = _as_values(A_shards)
     W = _as_values(W_shards)
@@ -95,13 +151,27 @@ def rank_partials(A_shards, W_shards) -> np.ndarray:
     return np.stack([A[r] @ W[r] for r in range(WORLD)])
 
 
-def reduce_partials(S: np.ndarray):
+def partials_bf16(A_shards, W_shards, S=None) -> np.ndarray:
+    """Each rank's partial rounded once to bf16 from its exact value:
+    Q_r = bf16(A_r @ W_r), [8][M][N].  S: rank_partials' result, if at hand."""
+    A = _as_values(A_shards)
+    W = _as_values(W_shards)
+    if S is None:
+        S = rank_partials(A, W)
+    return np.stack([bf16_of_exact_product(A[r], W[r], S[r]) for r in range(WORLD)])
+
+
+def reduce_partials(S: np.ndarray, Q=None):
     """Round each partial to bf16, fold in FP32 in rank order, round to bf16.
 
+    S: the partials (exact values, or rank_partials' float64 values); Q: their
+    bf16 roundings if already formed (partials_bf16), else bf16(S).
     Returns (out, ref): out [M][N] float64 values on the bf16 grid, ref [M][N]
-    the unrounded float64 sum of the exact partials.
+    the unrounded float64 sum of the partials.
     """
-    Q = [bf16_round(S[r]).astype(np.float32) for r in range(WORLD)]  # exact casts
+    if Q is None:
+        Q = [bf16_round(S[r]) for r in range(WORLD)]
+    Q = [np.asarray(Q[r]).astype(np.float32) for r in range(WORLD)]  # exact casts
     T = Q[0].copy()
     for r in range(1, WORLD):
         T = (T + Q[r]).astype(np.float32)  # IEEE fp32 add, round to nearest even
@@ -118,7 +188,8 @@ def gemm_rs(A_shards, W_shards):
     Returns (out, ref) as float64 arrays [M][N]; slice s of the reduce-scatter
     is rows [s*M/8, (s+1)*M/8) of out (see slices()).
     """
-    return reduce_partials(rank_partials(A_shards, W_shards))
+    S = rank_partials(A_shards, W_shards)
+    return reduce_partials(S, partials_bf16(A_shards, W_shards, S))
 
 
 def gemm_rs_rows(A_shards, W_shards, rows):
@@ -154,7 +225,7 @@ def ag_gemm(A_shards, W_shards):
     A = np.concatenate(list(_as_values(A_shards)), axis=0)
     Wv = _as_values(W_shards)
     ref = np.stack([A @ Wv[r] for r in range(Wv.shape[0])])
-    return bf16_round(ref), ref
+    return np.stack([bf16_of_exact_product(A, Wv[r], ref[r]) for r in range(Wv.shape[0])]), ref
 
 
 def ag_gemm_rows(A_shards, W_shards, rows):
@@ -163,7 +234,7 @@ def ag_gemm_rows(A_shards, W_shards, rows):
     A = np.concatenate(list(_as_values(A_shards)), axis=0)[np.asarray(rows, dtype=np.int64)]
     Wv = _as_values(W_shards)
     ref = np.stack([A @ Wv[r] for r in range(Wv.shape[0])])
-    return bf16_round(ref), ref
+    return np.stack([bf16_of_exact_product(A, Wv[r], ref[r]) for r in range(Wv.shape[0])]), ref
 
 
 def slices(out: np.ndarray, world: int = WORLD):

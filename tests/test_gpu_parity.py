@@ -27,7 +27,7 @@ def _full_check(A_bits, W_bits, check_partials=True, **kw):
     c = Case(A_bits, W_bits, **kw)
     fused = c.run(G.FUSED, poison=True)
     S = oracle.rank_partials(A_bits, W_bits)
-    out, ref = oracle.reduce_partials(S)
+    out, ref = oracle.reduce_partials(S, oracle.partials_bf16(A_bits, W_bits, S))
     fv = to_host_values(fused)
     assert_parity(fv, out, ref)
     if check_partials:  # the staging holds defined partials after GEMM_ONLY (not after FUSED)

@@ -37,7 +37,7 @@ def _check_workload(w):
     fused = c.run(G.FUSED, poison=True)
     rows = _sample_rows(w.M, w.seed)
     S = oracle.rank_partials(A[:, rows, :], W)
-    out, ref = oracle.reduce_partials(S)
+    out, ref = oracle.reduce_partials(S, oracle.partials_bf16(A[:, rows, :], W, S))
     fv = to_host_values(fused[torch.as_tensor(rows, device="cuda")])
     e = oracle.err_vs_oracle(fv, out)
     assert e <= TOL, f"{w.name}: sampled err {e:.3e}"

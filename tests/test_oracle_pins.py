@@ -228,6 +228,41 @@ def test_pipeline_matches_brute_force_wide_exponents():
                for i in range(M) for j in range(N))
 
 
+def test_partial_rounded_from_the_exact_value_not_the_float64_sum():
+    """Products 1, 2^-8 and 2^-70: the exact sum 1 + 2^-8 + 2^-70 lies just
+    above the bf16 midpoint 1 + 2^-8 and rounds up to 1 + 2^-7; the float64
+    sum drops 2^-70, lands on the midpoint and would round to even (1)."""
+    X = np.array([[1.0, 2.0 ** -4, 2.0 ** -35]])
+    Y = np.array([[1.0], [2.0 ** -4], [2.0 ** -35]])
+    assert oracle.bf16_round(X @ Y)[0, 0] == 1.0
+    assert oracle.bf16_of_exact_product(X, Y)[0, 0] == 1.0 + 2.0 ** -7
+    assert float(rbf16(Fraction(1) + Fraction(1, 2 ** 8) + Fraction(1, 2 ** 70))) == 1.0 + 2.0 ** -7
+    # the same through the whole layer: one rank holds these products
+    A = np.zeros((8, 8, 8)); W = np.zeros((8, 8, 8))
+    A[5, 0, :3] = X[0]; W[5, :3, 0] = Y[:, 0]
+    A_sh, W_sh = _bits_from_values(A), _bits_from_values(W)
+    out, _ = oracle.gemm_rs(A_sh, W_sh)
+    assert out[0, 0] == 1.0 + 2.0 ** -7
+    assert np.array_equal(out, brute_force(A_sh, W_sh))
+    C, _ = oracle.ag_gemm(_bits_from_values(np.tile(X, (8, 1)).reshape(8, 1, 3)),
+                          _bits_from_values(np.tile(Y, (8, 1, 8))))
+    assert np.all(C[:, :, 0] == 1.0 + 2.0 ** -7)
+
+
+def test_bf16_round_fraction_matches_independent_rounding():
+    g = np.random.Generator(np.random.PCG64(61))
+    for _ in range(3000):
+        num = int(g.integers(-2 ** 40, 2 ** 40))
+        den = 2 ** int(g.integers(0, 200)) * int(g.integers(1, 2 ** 12))
+        x = Fraction(num, den)
+        assert oracle.bf16_round_fraction(x) == float(rbf16(x)), x
+    for x in (Fraction(0), Fraction(2) ** 128, -Fraction(2) ** 130, Fraction(1, 2 ** 140),
+              Fraction(3, 2 ** 134), Fraction(2) ** 127 * Fraction(511, 256)):
+        r = rbf16(x)
+        want = float(r) if abs(r) < Fraction(2) ** 128 else float("inf") * (1 if x > 0 else -1)
+        assert oracle.bf16_round_fraction(x) == want, x
+
+
 # ---------------------------------------------------------------------------
 # closed forms and invariants
 # ---------------------------------------------------------------------------
@@ -423,3 +458,59 @@ def test_ag_gemm_rows_subset():
     rows = [0, 7, 8, 33, 63]
     Cr, _ = oracle.ag_gemm_rows(A_sh, W_sh, rows)
     assert np.array_equal(Cr, C[:, rows])
+
+
+# ---------------------------------------------------------------------------
+# Property-based: arbitrary finite bf16 inputs over a wide exponent range
+# (where the bf16 partial rounding and the fp32 fold both round), against the
+# exact rational brute force.
+
+
+def test_pipeline_matches_brute_force_on_arbitrary_bf16():
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    def bf16_value(sign, exp, mant):
+        return (-1) ** sign * (1 + mant / 128) * 2.0 ** exp
+
+    value = st.builds(bf16_value, st.integers(0, 1), st.integers(-40, 40), st.integers(0, 127))
+    entry = st.one_of(value, st.just(0.0))
+
+    @hyp.settings(max_examples=40, deadline=None, derandomize=True,
+                  phases=[hyp.Phase.explicit, hyp.Phase.generate])
+    @hyp.given(st.integers(1, 3), st.integers(1, 3),
+               st.lists(entry, min_size=8 * 8 * 3, max_size=8 * 8 * 3),
+               st.lists(entry, min_size=8 * 3 * 3, max_size=8 * 3 * 3))
+    def check(Kr, N, a_vals, w_vals):
+        A = np.array(a_vals[:8 * 8 * Kr]).reshape(8, 8, Kr)
+        W = np.array(w_vals[:8 * Kr * N]).reshape(8, Kr, N)
+        A_sh, W_sh = _bits_from_values(A), _bits_from_values(W)
+        out, _ = oracle.gemm_rs(A_sh, W_sh)
+        assert np.array_equal(out, brute_force(A_sh, W_sh))
+
+    check()
+
+
+def test_fold_order_matters_on_powers_of_two():
+    """Signed powers of two with K/8 = 1: every partial is one of ±1, ±2^13,
+    ±2^26 and exact in bf16, so the fp32 fold alone decides the result.
+    Next to 2^26 a 1 is absorbed (fp32 keeps 24 bits) and shows once the
+    large terms cancel, so the rank order and the fp32 width both matter: a
+    float64 fold or another order gives other results."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    term = st.builds(lambda s, e: (-1) ** s * 2.0 ** e, st.integers(0, 1),
+                     st.sampled_from([13, 0]))
+
+    @hyp.settings(max_examples=100, deadline=None, derandomize=True,
+                  phases=[hyp.Phase.explicit, hyp.Phase.generate])
+    @hyp.given(st.lists(term, min_size=8 * 8, max_size=8 * 8),
+               st.lists(term, min_size=8 * 4, max_size=8 * 4))
+    def check(a_vals, w_vals):
+        A = np.array(a_vals).reshape(8, 8, 1)
+        W = np.array(w_vals).reshape(8, 1, 4)
+        A_sh, W_sh = _bits_from_values(A), _bits_from_values(W)
+        out, _ = oracle.gemm_rs(A_sh, W_sh)
+        assert np.array_equal(out, brute_force(A_sh, W_sh))
+
+    check()
