@@ -514,3 +514,25 @@ def test_fold_order_matters_on_powers_of_two():
         assert np.array_equal(out, brute_force(A_sh, W_sh))
 
     check()
+
+
+def test_ag_gemm_matches_brute_force_on_arbitrary_bf16():
+    """All-gather GEMM on arbitrary finite bf16 inputs over exponents -40..40:
+    one rounding of the exact product, whatever the products' magnitudes."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    value = st.builds(lambda s, e, m: (-1) ** s * (1 + m / 128) * 2.0 ** e,
+                      st.integers(0, 1), st.integers(-40, 40), st.integers(0, 127))
+
+    @hyp.settings(max_examples=40, deadline=None, derandomize=True,
+                  phases=[hyp.Phase.explicit, hyp.Phase.generate])
+    @hyp.given(st.integers(1, 4), st.lists(value, min_size=8 * 4, max_size=8 * 4),
+               st.lists(value, min_size=8 * 4 * 2, max_size=8 * 4 * 2))
+    def check(K, a_vals, w_vals):
+        A = np.array(a_vals[:8 * K]).reshape(8, 1, K)      # one row per shard
+        W = np.array(w_vals[:8 * K * 2]).reshape(8, K, 2)  # two columns per rank
+        A_sh, W_sh = _bits_from_values(A), _bits_from_values(W)
+        C, _ = oracle.ag_gemm(A_sh, W_sh)
+        assert np.array_equal(C, _ag_brute_force(A_sh, W_sh))
+
+    check()
