@@ -34,8 +34,9 @@ C_r = A W_r, rounded once to bf16 from its exact value (the GPU accumulates
 in FP32, so parity there is a tolerance).
 
 Pins that tie this module to something other than itself live in
-tests/test_oracle_pins.py (exact rational brute force, closed forms, invariants
-and library routines).
+tests/test_oracle_pins.py (exact rational brute force, also on arbitrary
+wide-exponent inputs drawn by hypothesis, closed forms, invariants and
+library routines).
 """
 from __future__ import annotations
 

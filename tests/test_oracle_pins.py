@@ -1,7 +1,8 @@
 """Pins for the CPU oracle: it is checked against things other than itself.
 
   * exact rational brute force (fractions.Fraction) with an independent
-    round-to-nearest-even for bf16 and fp32, on tiny random shapes;
+    round-to-nearest-even for bf16 and fp32, on tiny random shapes and on
+    arbitrary wide-exponent inputs drawn by hypothesis;
   * torch's float32 -> bfloat16 conversion (a library routine) for the bf16
     rounding of float32 inputs;
   * closed forms: integer inputs (everything exact), identity weights,
