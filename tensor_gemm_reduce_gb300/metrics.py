@@ -98,3 +98,39 @@ def max_over_ranks(values: List[float], device=None) -> List[float]:
     t = torch.tensor(values, dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return [float(v) for v in t.cpu()]
+
+
+def timeline_tail(tl: Dict) -> Dict:
+    """Where a traced fused run spends its end, from Plan.timeline() (times in
+    microseconds from the earliest CTA start):
+      mma_p50 / mma_max  when the median / last CTA's MMA issue drained (the
+                         spread is the GEMM's own imbalance at the end);
+      last_queued        when the last reduce item was queued (the final
+                         tiles' epilogue and completion adds are done);
+      last_done, end     the last item reduced, the last CTA finished;
+      after_last_mma     items queued after the last MMA drained, and their
+                         median time from taken to done (item_us_late);
+      pickup_us, item_us medians over all items of queued -> taken and
+                         taken -> done.
+    Missing stamps (CTAs beyond the traced ones, items of other runs) are
+    skipped."""
+    ctas = [c for c in tl.get("ctas", []) if c.get("end") is not None]
+    mma = sorted(c["mma_drained"] for c in ctas if c.get("mma_drained") is not None)
+    items = [i for i in tl.get("items", [])
+             if None not in (i.get("queued"), i.get("taken"), i.get("done"))]
+    if not mma or not items:
+        raise ValueError("timeline has no MMA stamps or no complete reduce items")
+    mma_max = mma[-1]
+    late = [i for i in items if i["queued"] > mma_max]
+    return {
+        "mma_p50": median(mma),
+        "mma_max": mma_max,
+        "last_queued": max(i["queued"] for i in items),
+        "last_done": max(i["done"] for i in items),
+        "end": max(c["end"] for c in ctas),
+        "after_last_mma": len(late),
+        "item_us_late": median(i["done"] - i["taken"] for i in late) if late else 0.0,
+        "pickup_us": median(i["taken"] - i["queued"] for i in items),
+        "item_us": median(i["done"] - i["taken"] for i in items),
+        "items": len(items),
+    }

@@ -46,6 +46,24 @@ def test_summarize_clocks():
     assert s["rejected"]
 
 
+def test_timeline_tail():
+    tl = {"ctas": [{"start": 0.0, "epilogue_done": 9.0, "mma_drained": 8.0, "end": 12.0},
+                   {"start": 0.1, "epilogue_done": 11.0, "mma_drained": 10.0, "end": 13.5},
+                   {"start": 0.2, "epilogue_done": 7.0, "mma_drained": 6.0, "end": 12.5},
+                   {"start": None, "epilogue_done": None, "mma_drained": None, "end": None}],
+          "items": [{"item": 0, "queued": 2.0, "taken": 3.0, "done": 5.0},
+                    {"item": 1, "queued": 10.5, "taken": 11.0, "done": 12.0},
+                    {"item": 2, "queued": 11.0, "taken": 11.5, "done": 13.0},
+                    {"item": 3, "queued": None, "taken": None, "done": None}]}
+    t = metrics.timeline_tail(tl)
+    assert t["mma_p50"] == 8.0 and t["mma_max"] == 10.0
+    assert t["last_queued"] == 11.0 and t["last_done"] == 13.0 and t["end"] == 13.5
+    assert t["after_last_mma"] == 2 and t["item_us_late"] == 1.25
+    assert t["pickup_us"] == 0.5 and t["item_us"] == 1.5 and t["items"] == 3
+    with pytest.raises(ValueError):
+        metrics.timeline_tail({"ctas": [], "items": []})
+
+
 def _rank_main(rank, world, port, q):
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
