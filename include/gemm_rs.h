@@ -101,7 +101,8 @@ enum gemm_rs_mode {
 #define GEMM_RS_DEBUG_NO_STAGING_L2 0x2u /* FUSED: store staging tiles without the L2
                                             evict-last hint and keep them after reduction
                                             (by default reduced staging lines are dropped
-                                            from L2 unwritten; needs N % 64 == 0) */
+                                            from L2 unwritten when N % 64 == 0 and the
+                                            workspace is 128-byte aligned) */
 #define GEMM_RS_DEBUG_TRACE 0x4u         /* GEMM kernels write, per CTA, four global-timer
                                             stamps (ns, u64): start, epilogue done with its
                                             tiles, MMA issue drained, all warps done; at
@@ -129,9 +130,9 @@ typedef struct gemm_rs_desc {
   int32_t unit_rows;      /* rows per reduce item in FUSED mode: 4, 8, 16 or 32; 0 = 8 */
   uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
   uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
-  int32_t mma_ctas;       /* CTAs of a cluster sharing one tile: 1 (128 x 256 tiles), 2 (a
-                             2-CTA MMA, 256 x 256 tiles) or 4 (two 2-CTA MMAs, 512 x 256
-                             tiles, W tiles shared by TMA multicast); 0 = 2 */
+  int32_t mma_ctas;       /* CTAs of a cluster sharing one tile: 1 (128 x 256 tiles) or 2
+                             (a 2-CTA MMA, 256 x 256 tiles); 0 = 2.  Every CTA loads its
+                             own operand tiles (no load is multicast between CTAs) */
   int32_t chunks;         /* CHUNKED: row chunks, 1..64; 0 = 4 (each a whole number of tile
                              rows, the last one ragged) */
   int32_t replicas;       /* copies of the reduced output: 0 or 1 = reduce-scatter, out is
@@ -191,12 +192,15 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
  * Enqueue one execution on `stream` (a cudaStream_t; NULL = legacy default).
  * A: [8][M][K/8] bf16, W: [8][K/8][N] bf16, out: [M][N] bf16 ([8][M][N] with
  * replicas = 8), workspace:
- * >= workspace_bytes, 256-byte aligned is best, 16-byte aligned is required.
+ * >= workspace_bytes, 16-byte aligned; at a 128-byte boundary (torch and
+ * cudaMalloc allocations are) FUSED also keeps the staging in L2 and drops
+ * each reduced line unwritten, which is faster; at other 16-byte offsets the
+ * staging is written back as in the unfused path.
  * The caller may pass an uninitialised workspace: the first call that sees a
  * new workspace pointer clears its control words (a small memset on the
  * stream).  After GEMM_ONLY or UNFUSED the staging part holds the per-rank
  * partials of that GEMM; after FUSED it holds no defined values (reduced
- * staging lines are dropped from L2 without write-back when N % 64 == 0).
+ * staging lines are dropped from L2 without write-back, see above).
  * Returns after enqueueing; device-side failures (timeouts) are reported by
  * gemm_rs_status.  CHUNKED also uses a second stream and events that the plan
  * creates on its first CHUNKED call; that stream joins `stream` again before

@@ -75,7 +75,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->unit_rows != 0 && d->unit_rows != 4 && d->unit_rows != 8 && d->unit_rows != 16 &&
       d->unit_rows != 32)
     return GEMM_RS_ERR_INVALID_ARG;
-  if (d->mma_ctas < 0 || d->mma_ctas == 3 || d->mma_ctas > 4) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->mma_ctas < 0 || d->mma_ctas > 2) return GEMM_RS_ERR_INVALID_ARG;
   if (d->chunks < 0 || d->chunks > kMaxChunks) return GEMM_RS_ERR_INVALID_ARG;
   if (d->replicas != 0 && d->replicas != 1 && d->replicas != kWorld) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op != GEMM_RS_OP_RS && d->op != GEMM_RS_OP_AG) return GEMM_RS_ERR_INVALID_ARG;
@@ -149,10 +149,9 @@ long long items_of(long long blocks, int blocks_per_region, long long tail_regio
 }
 
 // kind: Kind (GEMM only, fused reduce-scatter, fused all-gather); ctas: CTAs
-// of the cluster that share a tile (1, 2 or 4).
+// of the cluster that share a tile (1 or 2).
 template <int kKind>
 const void* kernel_for(int ctas) {
-  if (ctas == 4) return reinterpret_cast<const void*>(gemm_rs_kernel<kKind, 4>);
   if (ctas == 2) return reinterpret_cast<const void*>(gemm_rs_kernel<kKind, 2>);
   return reinterpret_cast<const void*>(gemm_rs_kernel<kKind, 1>);
 }
@@ -163,8 +162,7 @@ const void* gemm_kernel(int kind, int ctas) {
 }
 
 int gemm_smem(int ctas) {
-  return ctas == 4 ? TileCfg<4>::kSmemAlloc
-                   : ctas == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc;
+  return ctas == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc;
 }
 
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, int kind,
@@ -206,7 +204,7 @@ int launch_gemm_kernel(int pair, int kind, int grid, int threads, const GemmPara
 // Set the shared-memory limit of the GEMM kernels; persistent grid size
 // (CTAs) for `pair` CTAs per MMA: one CTA per SM, whole clusters only.
 int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_fused, int* grid) {
-  for (int pr = 1; pr <= 4; pr *= 2)
+  for (int pr = 1; pr <= 2; ++pr)
     for (int kind = kKindGemm; kind <= kKindAG; ++kind)
       if (cudaFuncSetAttribute(gemm_kernel(kind, pr), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                gemm_smem(pr)) != cudaSuccess) {
@@ -860,7 +858,12 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
   int rc = GEMM_RS_OK;
   switch (mode) {
     case GEMM_RS_FUSED:
-      h->params.staging_in_l2 = (d.N % 64 == 0) && !(d.debug_flags & GEMM_RS_DEBUG_NO_STAGING_L2);
+      // The reducers drop whole 128-byte staging lines from L2: only when every
+      // line holds one reduce unit's columns (N % 64 == 0 and the staging base on
+      // a 128-byte boundary); otherwise a dropped line could take unreduced
+      // bytes of a neighbouring unit with it.
+      h->params.staging_in_l2 = (d.N % 64 == 0) && (reinterpret_cast<uintptr_t>(wsb) & 127u) == 0 &&
+                                !(d.debug_flags & GEMM_RS_DEBUG_NO_STAGING_L2);
       h->epoch += 1;
       h->params.epoch = h->epoch;
       // every epilogue warp of every rank adds 1 per block and run
@@ -1068,6 +1071,7 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
                   kBK))
       return GEMM_RS_ERR_CUDA;
     p.stage = reinterpret_cast<uint16_t*>(scratch);
+    p.staging_in_l2 = (N % 64 == 0);  // as a default plan: the array is 256-byte aligned
     p.plane = M * N;
     p.replicas = 1;
     p.out_stride = M * N;

@@ -59,13 +59,14 @@ constexpr int kGemmWarps = 2 + kEpiWarps;
 constexpr int kMaxReducerWarps = 6;
 
 // Shared-memory plan of one CTA.  kCtas = CTAs of the cluster that share a
-// tile: 1 (one-CTA MMA), 2 (one 2-CTA MMA) or 4 (two 2-CTA MMAs on vertically
-// adjacent 256-row halves of the tile, sharing its W tile by TMA multicast).
+// tile: 1 (one-CTA MMA) or 2 (one 2-CTA MMA).  Every CTA loads its own
+// operands; no load is shared between CTAs.
 // The epilogue needs no shared memory, so all of it but the barriers holds
 // operand stages: the loads are latency-bound, and each stage more hides more.
 template <int kCtas>
 struct TileCfg {
-  static constexpr int kPair = kCtas >= 2 ? 2 : 1;     // CTAs per MMA
+  static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair per tile");
+  static constexpr int kPair = kCtas;                  // CTAs per MMA
   static constexpr int kStages = kCtas == 1 ? 4 : 7;
   static constexpr int kTileRows = kBM * kCtas;        // output rows of one cluster tile
   static constexpr int kBCols = kBN / kPair;           // W columns held by one CTA
@@ -162,8 +163,9 @@ struct GemmParams {
   uint32_t debug_flags;
   // Fused kernel only: staging tiles are stored with an L2 evict-last hint so
   // they are still in L2 when reduced, and each reduced staging line is
-  // discarded from L2 (never written back).  Needs N % 64 == 0 so that no
-  // 128-byte line holds data of two reduce units.
+  // discarded from L2 (never written back).  Needs N % 64 == 0 and a staging
+  // base on a 128-byte boundary, so that no 128-byte line holds data of two
+  // reduce units.
   uint32_t staging_in_l2;
   // Adaptive reducer share (mKernel page, section 3.2): a controller thread
   // publishes how many of each CTA's reducer warps take items; the others wait.
@@ -566,7 +568,7 @@ template <int kCtas>
 struct TileRing {
   static constexpr int kDepth = 4;
   static constexpr uint32_t kConsumers =
-      kCtas == 1 ? 1 + kEpiWarps : kCtas == 2 ? 2 + 2 * kEpiWarps : 2 + 4 * kEpiWarps + 3;
+      kCtas == 1 ? 1 + kEpiWarps : 2 + 2 * kEpiWarps;
   uint32_t slots;   // shared address of int32 slot[kDepth]
   uint32_t full;    // shared address of mbarrier full[kDepth]
   uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in CTA 0)
@@ -651,9 +653,8 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
     for (int s = 0; s < C::kStages; ++s) {
       // the MMA leader's expect-tx arrival (+ the bytes landing in its pair)
       mbar_init(bar_full + 8 * s, 1);
-      // one MMA commit per MMA pair writing into this stage (4 CTAs: both pairs,
-      // since both pairs' W loads land in every CTA)
-      mbar_init(bar_empty + 8 * s, kCtas == 4 ? 2 : 1);
+      // one MMA commit frees the stage
+      mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_acc_full + 8 * b, 1);
@@ -737,7 +738,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
           }
         }
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!bar_wait<kCtas == 4>(bar_empty + 8 * stage, phase ^ 1u, limit, cta_abort)) {
+          if (!bar_wait(bar_empty + 8 * stage, phase ^ 1u, limit, cta_abort)) {
             if (!*cta_abort) {
               record_error(p, kErrPipeTimeout, kWhereTma, (uint32_t)idx);
               *cta_abort = 1;
@@ -754,7 +755,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
 #pragma unroll
             for (int j = 0; j < C::kBBoxes; ++j)
               tma_load_3d(sb + j * C::kBBoxBytes, &p.tmap_b, fb, n0 + 64 * j, kb * kBK, tc.rank);
-          } else if constexpr (kCtas == 2) {
+          } else {
             // both CTAs' bytes are counted on the leader's barrier
             if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
             const uint32_t fb_leader = mapa_shared(fb, 0);
@@ -763,18 +764,6 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
             for (int j = 0; j < C::kBBoxes; ++j)
               tma_load_3d_pair(sb + j * C::kBBoxBytes, &p.tmap_b, fb_leader, n0 + 64 * j,
                                kb * kBK, tc.rank);
-          } else {
-            // each pair's leader counts the bytes landing in both CTAs of its
-            // pair: the CTAs' own A rows and the two 64-column W boxes of each
-            // CTA's column half, one loaded by each pair and multicast to the
-            // CTAs of both pairs that hold that half
-            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
-            const uint32_t fb_leader = mapa_shared(fb, mma_leader_rank);
-            tma_load_3d_pair(sa, amap, fb_leader, kb * kBK, arow, tc.rank);
-            const uint32_t pair_id = cta_rank >> 1;
-            const uint16_t mask = (uint16_t)((1u << half) | (1u << (half + 2)));
-            tma_load_3d_pair_multicast(sb + pair_id * C::kBBoxBytes, &p.tmap_b, fb_leader,
-                                       n0 + 64 * (int)pair_id, kb * kBK, tc.rank, mask);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -841,11 +830,11 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
             const uint64_t bd = smem_desc_sw128(sb + s * 2048, C::kBBoxBytes, 1024);
             mma_bf16<kPair>(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
           }
-          // frees the smem stage (in every CTA a W load wrote into) when these MMAs finish
+          // frees the smem stage (in both CTAs of the pair) when these MMAs finish
           if constexpr (kCtas == 1)
             mma_commit<1>(bar_empty + 8 * stage);
           else
-            mma_commit_pair_multicast(bar_empty + 8 * stage, kCtas == 4 ? 0xF : 0x3);
+            mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -856,7 +845,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
         if constexpr (kCtas == 1)
           mma_commit<1>(bar_acc_full + 8 * acc);
         else
-          mma_commit_pair_multicast(bar_acc_full + 8 * acc, (uint16_t)(0x3u << mma_leader_rank));
+          mma_commit_pair_multicast(bar_acc_full + 8 * acc, 0x3);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }

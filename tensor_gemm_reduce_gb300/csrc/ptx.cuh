@@ -137,20 +137,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cluster_bar)
       : "memory");
 }
-// 3-D tiled load multicast to the CTAs of cta_mask for CTA pairs: the bytes
-// landing in each destination CTA are counted on the mbarrier at the given
-// offset in that destination's pair leader.
-__device__ __forceinline__ void tma_load_3d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           uint32_t cluster_bar, int c0, int c1,
-                                                           int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cluster_bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // 16-byte global store; with an L2 cache policy (createpolicy) in the _hint form.
 __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),

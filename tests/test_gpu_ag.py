@@ -89,7 +89,6 @@ def test_tiny_workload():
     (1024, 1024, 512, {}, False),                  # 128-row shards inside 256-row tiles
     (392, 1536, 1600, {}, False),                  # ragged M and K; 49-row shards
     (8, 512, 64, {}, False),                       # one row per shard
-    (1024, 1536, 2048, dict(mma_ctas=4), False),   # 512-row tiles over 128-row shards
     (2048, 2560, 1024, dict(reducer_warps=1, grid=6), True),  # one copy warp, few CTAs
     (2048, 2560, 1024, dict(reducer_warps=6), True),
     (2048, 4096, 512, dict(grid=8), True),   # 16 tiles per rank >= 2 waves of 4 clusters: paced copies

@@ -41,7 +41,7 @@ def _full_check(A_bits, W_bits, check_partials=True, **kw):
     return c, fv, out
 
 
-@pytest.mark.parametrize("ctas", [1, 2, 4])
+@pytest.mark.parametrize("ctas", [1, 2])
 def test_tiny_workload(ctas):
     A, W = workloads.make_inputs(workloads.TINY)
     _full_check(A, W, mma_ctas=ctas)
@@ -58,7 +58,6 @@ def test_ragged_and_small_shapes(M, N, K):
     A, W = workloads.make_shape_inputs(M, N, K, seed=M + N + K)
     _full_check(A, W)
     _full_check(A, W, mma_ctas=1)
-    _full_check(A, W, mma_ctas=4)
 
 
 @pytest.mark.parametrize("kw", [dict(reducer_warps=1), dict(reducer_warps=6), dict(grid=3),
@@ -68,7 +67,7 @@ def test_ragged_and_small_shapes(M, N, K):
                                 dict(mma_ctas=1), dict(mma_ctas=1, unit_rows=32, grid=5),
                                 dict(mma_ctas=1, unit_rows=8, reducer_warps=1),
                                 dict(mma_ctas=2, band_m=1, unit_rows=32),
-                                dict(mma_ctas=4), dict(mma_ctas=4, grid=8, reducer_warps=2),
+                                dict(grid=8, reducer_warps=2),
                                 dict(adaptive=1), dict(adaptive=1, reducer_warps=6, unit_rows=8),
                                 dict(adaptive=1, mma_ctas=1, grid=5),
                                 dict(unit_rows=4, tail_waves=1), dict(unit_rows=16, tail_waves=64)])
@@ -84,7 +83,7 @@ def test_plan_variants(kw):
     (1024, 1280, 2048, dict(chunks=3)),              # 3 chunks: 512, 512 and none -> 2 used
     (392, 776, 1600, dict(chunks=2)),                # ragged M, N, K; last chunk 136 rows
     (392, 776, 1600, dict(chunks=8, mma_ctas=1)),    # 128-row tiles: chunks of 128, 128, 128, 8
-    (2048, 512, 1024, dict(chunks=8, mma_ctas=4)),   # 512-row tiles: 4 chunks
+    (2048, 512, 1024, dict(chunks=8)),               # 256-row tiles: 8 chunks
     (8, 256, 512, dict(chunks=4)),                   # one chunk of 8 rows
     (520, 1000, 1024, dict(chunks=1, band_m=1)),     # a single chunk is the unfused path
 ])
@@ -131,7 +130,7 @@ def test_chunked_zero_k_and_host_copies():
     (392, 776, 1600, {}),                 # ragged M, N and K
     (264, 1536, 2048, {}),                # N % 64 == 0: staging kept in L2 and dropped
     (1024, 1280, 2048, dict(mma_ctas=1)),
-    (2048, 512, 1024, dict(mma_ctas=4, chunks=3)),
+    (2048, 512, 1024, dict(chunks=3)),
     (8, 256, 512, {}),                    # one row per rank's slice
 ])
 def test_allreduce_copies_equal_reduce_scatter(M, N, K, kw):
@@ -419,3 +418,29 @@ def test_pure_c_caller(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "exact" in r.stdout
+
+
+@pytest.mark.parametrize("offset", [16, 48, 128])
+def test_fused_on_workspace_off_a_line_boundary(offset):
+    """The ABI asks for a 16-byte aligned workspace.  At an offset that is not
+    a multiple of 128 bytes the fused run must not drop staging lines from L2
+    (a dropped line would span two reduce units): it must still equal the
+    unfused run bit for bit, repeatedly, with N % 64 == 0."""
+    M, N, K = 1024, 1536, 2048
+    A, W = workloads.make_shape_inputs(M, N, K, seed=95)
+    plan = G.Plan(M, N, K)
+    big = torch.empty(plan.workspace_bytes + 256, dtype=torch.uint8, device="cuda")
+    ws = big[offset:offset + plan.workspace_bytes]
+    assert ws.data_ptr() % 16 == 0
+    Ad, Wd = to_dev(A), to_dev(W)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    plan.run(Ad, Wd, out, ws, G.UNFUSED)
+    assert plan.status() == G.GEMM_RS_OK
+    ref = out.clone()
+    for _ in range(4):
+        out.view(torch.int16).fill_(-1)
+        plan.run(Ad, Wd, out, ws, G.FUSED)
+        assert plan.status() == G.GEMM_RS_OK
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    exp, _ = oracle.gemm_rs(A, W)
+    assert_parity(to_host_values(out), exp, None)
