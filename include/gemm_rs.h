@@ -108,11 +108,12 @@ enum gemm_rs_mode {
                                             tiles, MMA issue drained, all warps done; at
                                             workspace + gemm_rs_info.trace_offset (up to
                                             1024 CTAs).  The fused reduce-scatter also
-                                            stamps every reduce item when it was queued,
-                                            taken and done: u64 words 1..3 of its 32-byte
-                                            slot at workspace + gemm_rs_info.queue_offset
-                                            (word 0 holds run << 32 | item, item = 128-row
-                                            block << 5 | part) */
+                                            stamps every reduce item when its block became
+                                            complete, when a reducer saw that and when it was
+                                            done: u64 words 1..3 of a 32-byte slot per item
+                                            (items in the order they are reduced) at workspace
+                                            + gemm_rs_info.queue_offset (word 0 holds run << 32
+                                            | item, item = 128-row block << 5 | part) */
 
 /*
  * Problem description.  Shapes: A is [8][M][K/8] bf16 (row-major, K/8
@@ -157,7 +158,7 @@ typedef struct gemm_rs_info {
   int32_t grid;           /* CTAs of the GEMM / fused kernels */
   int32_t threads_fused;  /* threads per CTA of the fused kernel */
   int32_t threads_gemm;   /* threads per CTA of the unfused GEMM kernel */
-  int32_t smem_bytes;     /* dynamic shared memory per CTA of both GEMM kernels */
+  int32_t smem_bytes;     /* dynamic shared memory per CTA of the GEMM kernels (largest) */
   int32_t band_m;         /* tile-order band height in m-tiles */
   int32_t unit_rows;      /* rows per reduce unit (FUSED) */
   int32_t mt, nt;         /* tile rows (of tile_rows rows) and 256-column tiles of the output */
@@ -174,14 +175,14 @@ typedef struct gemm_rs_info {
   int32_t op;             /* GEMM_RS_OP_RS or GEMM_RS_OP_AG */
   int32_t ag_direct;      /* AG: own shard read from the input, not copied */
   int64_t copy_items;     /* AG: copy items of a fused run */
-  int64_t queue_offset;   /* byte offset of the reduce-item FIFO in the workspace */
+  int64_t queue_offset;   /* byte offset of the reduce items' debug stamps in the workspace */
 } gemm_rs_info;
 
 /*
  * Validate d and build a plan for the current CUDA device.  On success
  * *plan is set and *workspace_bytes (may be NULL) receives the size of the
  * device workspace every gemm_rs_run call needs: the bf16 staging regions
- * (8*M*N*2 bytes), the per-block completion counts, the reduce-item FIFO and
+ * (8*M*N*2 bytes), the per-block completion counts, the reduce items' stamps and
  * a few control words.  Arguments are
  * checked before any CUDA call, so INVALID_ARG / UNSUPPORTED_SHAPE come back
  * on a machine without a GPU too.

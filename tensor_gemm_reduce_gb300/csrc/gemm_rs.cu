@@ -21,7 +21,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kDefaultReducerWarps = 4;
 constexpr int kDefaultCopyWarps = 2;
 // Reduce item size: small items leave less reduction in service when the
-// last tiles finish, large ones cost fewer FIFO operations where the
+// last tiles finish, large ones cost fewer item operations where the
 // reduction is a large share of the work.  8-row items, and 4-row items for
 // the regions of the last 3 waves, were the best compromise measured (o_proj
 // fused 211 -> 206 us, M = 512 78 -> 72 us against 16-row items and a
@@ -40,7 +40,7 @@ struct Layout {
 };
 
 // blocks: 32-row blocks of the output (completion counts); items: reduce items
-// of a run (FIFO slots)
+// of a run (debug stamp slots)
 Layout layout_for(int64_t M, int64_t N, int64_t blocks, int64_t items) {
   Layout l;
   l.staging_bytes = (size_t)kWorld * (size_t)M * (size_t)N * 2;
@@ -161,8 +161,22 @@ const void* gemm_kernel(int kind, int ctas) {
   return kernel_for<kKindGemm>(ctas);
 }
 
-int gemm_smem(int ctas) {
-  return ctas == 2 ? TileCfg<2>::kSmemAlloc : TileCfg<1>::kSmemAlloc;
+template <int kKind>
+int smem_for(int ctas) {
+  return ctas == 2 ? TileCfg<kKind, 2>::kSmemAlloc : TileCfg<kKind, 1>::kSmemAlloc;
+}
+// Dynamic shared memory of the GEMM kernel of a Kind (stage counts differ).
+int gemm_smem(int kind, int ctas) {
+  if (kind == kKindRS) return smem_for<kKindRS>(ctas);
+  if (kind == kKindAG) return smem_for<kKindAG>(ctas);
+  return smem_for<kKindGemm>(ctas);
+}
+// The largest of them (what a plan needs from the device).
+int gemm_smem_max(int ctas) {
+  int m = gemm_smem(kKindGemm, ctas);
+  for (int k = kKindRS; k <= kKindAG; ++k)
+    if (gemm_smem(k, ctas) > m) m = gemm_smem(k, ctas);
+  return m;
 }
 
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, int kind,
@@ -170,11 +184,10 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pair, i
   memset(cfg, 0, sizeof(*cfg));
   cfg->gridDim = dim3((unsigned)grid);
   cfg->blockDim = dim3((unsigned)threads);
-  cfg->dynamicSmemBytes = (size_t)gemm_smem(pair);
+  cfg->dynamicSmemBytes = (size_t)gemm_smem(kind, pair);
   cfg->stream = st;
   // No co-residency is needed: GEMM tiles are claimed from an atomic ticket
   // by whichever CTAs run, and producers never wait for reducers.
-  (void)kind;
   int n = 0;
   if (pair > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
@@ -207,7 +220,7 @@ int prepare_kernels(int dev, int num_sms, int pair, int requested, int threads_f
   for (int pr = 1; pr <= 2; ++pr)
     for (int kind = kKindGemm; kind <= kKindAG; ++kind)
       if (cudaFuncSetAttribute(gemm_kernel(kind, pr), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               gemm_smem(pr)) != cudaSuccess) {
+                               gemm_smem(kind, pr)) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_RS_ERR_CUDA;
       }
@@ -328,7 +341,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   }
   if (prop.major != 10 || prop.minor != 3) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
   const int pair = mma_ctas_of(d);
-  if (prop.sharedMemPerBlockOptin < (size_t)gemm_smem(pair)) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
+  if (prop.sharedMemPerBlockOptin < (size_t)gemm_smem_max(pair)) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
   // reducer warps (reduce-scatter) or copy warps (all-gather: 2 keep the
   // copies ahead of the tiles with the least interference)
   const int reducer_warps = d->reducer_warps > 0 ? d->reducer_warps
@@ -405,7 +418,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->grid = h->grid;
   info->threads_fused = 32 * (kGemmWarps + h->reducer_warps);
   info->threads_gemm = 32 * kGemmWarps;
-  info->smem_bytes = gemm_smem(h->pair);
+  info->smem_bytes = gemm_smem_max(h->pair);
   info->band_m = h->band;
   info->unit_rows = h->unit_rows;
   info->mt = h->mt;
@@ -967,7 +980,7 @@ extern "C" int gemm_rs_run_host(gemm_rs_t h, int mode, const void* A_host, const
 // cudaGetSymbolAddress while that device is current and keeps it.
 namespace {
 constexpr size_t kNoallocStagingBytes = (size_t)32 << 20;  // 8*M*N*2 <= 32 MiB
-constexpr size_t kNoallocFlagBytes = (size_t)4 << 20;      // completion counts + item FIFO
+constexpr size_t kNoallocFlagBytes = (size_t)4 << 20;      // completion counts + item stamps
 constexpr size_t kNoallocCtrlBytes = (size_t)kCtrlWords * 4;
 constexpr size_t kNoallocBytes = kNoallocStagingBytes + kNoallocFlagBytes + kNoallocCtrlBytes;
 constexpr int kNoallocMaxDevices = 64;
@@ -1079,7 +1092,7 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.flags = flags;
     p.queue = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(flags) +
                                                     align_up(count_bytes, 256));
-    p.epoch = 1;  // the FIFO slots were just cleared (tag 0)
+    p.epoch = 1;  // first run on the counts just cleared
     p.ctrl = ctrl;
     p.M = (int)M;
     p.N = (int)N;

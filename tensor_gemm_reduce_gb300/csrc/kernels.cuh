@@ -26,11 +26,11 @@
 //                 coalesced stores into the rank's staging region (every store
 //                 instruction writes four whole 128-byte row segments); then
 //                 (fused kernel) each warp publishes its 32 rows with a release
-//                 add on the 128-row block's completion count; the add that
-//                 completes a block (the last of 8 ranks x 4 warps) appends the
-//                 block's reduce items to a global FIFO
-//   warps 6..     reducers (fused reduce-scatter): take the next FIFO
-//                 position, wait (acquire) until its item is there, add the 8
+//                 add on the 128-row block's completion count (8 ranks x 4
+//                 warps = 32 adds per block and run)
+//   warps 6..     reducers (fused reduce-scatter): take the next reduce item
+//                 in the order the tiles complete (one atomic ticket), wait
+//                 (acquire) until its block's count is complete, add the 8
 //                 bf16 partials in fp32 in rank order, write bf16 output (to
 //                 every rank's copy for the all-reduce).  The epilogue warps
 //                 join them when the CTA's tiles are done; optionally a
@@ -61,13 +61,17 @@ constexpr int kMaxReducerWarps = 6;
 // Shared-memory plan of one CTA.  kCtas = CTAs of the cluster that share a
 // tile: 1 (one-CTA MMA) or 2 (one 2-CTA MMA).  Every CTA loads its own
 // operands; no load is shared between CTAs.
-// The epilogue needs no shared memory, so all of it but the barriers holds
-// operand stages: the loads are latency-bound, and each stage more hides more.
-template <int kCtas>
+// The epilogue needs no shared memory, so the operand stages may take all of
+// it but the barriers.  The GEMM alone and the all-gather use 7 stages; the
+// fused reduce-scatter uses 6: every stage in flight also queues in front of
+// the reducers' loads and the epilogue's stores in the memory system, and
+// with 6 the fused run is faster (o_proj 206 -> 203 us, 2048 x 6144 x 6144
+// 143 -> 139 us) while the GEMM alone loses about 1%.
+template <int kKind, int kCtas>
 struct TileCfg {
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair per tile");
   static constexpr int kPair = kCtas;                  // CTAs per MMA
-  static constexpr int kStages = kCtas == 1 ? 4 : 7;
+  static constexpr int kStages = kCtas == 1 ? 4 : (kKind == kKindRS ? 6 : 7);
   static constexpr int kTileRows = kBM * kCtas;        // output rows of one cluster tile
   static constexpr int kBCols = kBN / kPair;           // W columns held by one CTA
   static constexpr int kBBoxes = kBCols / 64;          // 64-column TMA boxes per stage
@@ -90,8 +94,8 @@ struct TileCfg {
 // control words in the workspace
 enum CtrlWord : int {
   kCtrlReduced = 0,  // reduce items finished in this run (checked by the last CTA)
-  kCtrlQueueTail = 7,  // next FIFO position to fill
-  kCtrlQueueHead = 8,  // next FIFO position to take
+  kCtrlQueueTail = 7,  // unused (kept zero)
+  kCtrlQueueHead = 8,  // next reduce item to take (a position in the item order)
   kCtrlDone = 1,     // CTAs finished (the last one resets the words above and below)
   kCtrlAbort = 2,    // set when some warp gave up waiting
   kCtrlError = 3,    // error bits (kErr*), cleared by the host
@@ -102,12 +106,12 @@ enum CtrlWord : int {
   kCtrlTarget = 10,    // adaptive: reducer warps per CTA that take items (0 = all)
   kCtrlCount = 16
 };
-// Every control word, completion count and FIFO slot sits in its own part of
+// Every control word, completion count and item stamp slot sits in its own part of
 // a cache line, so atomics and polls on one do not queue behind another's.
 constexpr int kCtrlStride = 32;   // words: one 128-byte line per control word
 constexpr int kCtrlWords = kCtrlCount * kCtrlStride;
 constexpr int kFlagStride = 32;   // words: one 128-byte line per block count
-constexpr int kQueueStride = 4;   // 8-byte slots: one 32-byte sector per slot
+constexpr int kQueueStride = 4;   // 8-byte words per item's debug stamps (one 32-byte sector)
 enum ErrBits : uint32_t { kErrFlagTimeout = 1u, kErrPipeTimeout = 2u, kErrIncomplete = 4u };
 enum ErrWhere : uint32_t {
   kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereReducer = 4, kWhereShard = 5
@@ -150,13 +154,17 @@ struct GemmParams {
   int unit_rows;          // rows per reduce item: 8, 16 or 32
   int splits;             // reduce items per 128-row block (128 / unit_rows)
   int blocks_per_region;  // tile_rows / 128
-  // Regions from tail_region on are completed by the last wave of tiles: their
-  // blocks are cut into 4-row items so the reduction after the last tile is
-  // spread over many warps.  An item is (block << 5) | part.
+  // Reduce items are taken in the order the regions complete (the tile order
+  // of schedule.h, region after region).  Regions from order position
+  // tail_region on are completed by the last waves of tiles: their blocks are
+  // cut into 4-row items so the reduction after the last tile is spread over
+  // many warps.  Item positions: tail_region * blocks_per_region * splits
+  // unit_rows-row items, then 32 4-row items per block of the tail regions.
   int tail_region;
   long long num_tiles;
   long long num_items;    // reduce items of a run
-  // FIFO of reduce items, one slot per item of a run: slot = (epoch << 32) | item
+  // Debug stamps of each item (GEMM_RS_DEBUG_TRACE only), kQueueStride words
+  // per item position: (epoch << 32) | item, queued, taken, done.
   unsigned long long* queue;
   uint32_t epoch;         // fused runs on this workspace so far, this one included
   uint32_t flag_target;
@@ -232,50 +240,90 @@ __device__ __forceinline__ uint4 reduce8(const uint4 (&v)[kWorld]) {
   return o;
 }
 
-// Append the items (block << 5) | 0..parts-1 to the global FIFO.  Called by
-// the thread whose add completed the block, right after its acquire-release
-// fence: the fence plus these relaxed stores release the block to whoever
-// acquires a slot.  One add reserves all the positions.
-__device__ __forceinline__ void queue_push_block(const GemmParams& p, int block, int parts) {
-  const uint32_t pos = atomicAdd(p.ctrl + kCtrlQueueTail * kCtrlStride, (uint32_t)parts);
-  const uint64_t now = p.trace ? globaltimer_ns() : 0;
-  for (int sp = 0; sp < parts; ++sp) {
-    unsigned long long* slot = p.queue + (size_t)(pos + sp) * kQueueStride;
-    if (p.trace) st_relaxed_gpu_u64(slot + 1, now);  // debug timeline: queued
-    st_relaxed_gpu_u64(slot, ((uint64_t)p.epoch << 32) | (uint32_t)((block << 5) | sp));
+// A reduce item: rows [row_begin, row_begin + rows) of a 128-row block.
+struct Item {
+  int block;  // 128-row block: (physical region) * blocks_per_region + CTA of the pair
+  int part;   // which rows of the block
+  int rows;   // unit_rows, or 4 in the tail regions
+};
+
+// The item at order position pos (0 <= pos < num_items): regions in the order
+// the tiles complete them (tile_at's region order), each region's blocks in
+// turn, each block's parts in turn.
+__device__ __forceinline__ Item item_at(const GemmParams& p, long long pos) {
+  const long long per_region = (long long)p.blocks_per_region * p.splits;
+  const long long tail_start = (long long)p.tail_region * per_region;
+  long long g, r;
+  int per_block;
+  Item it;
+  if (pos < tail_start) {
+    g = pos / per_region;
+    r = pos - g * per_region;
+    per_block = p.splits;
+    it.rows = p.unit_rows;
+  } else {
+    const long long q = pos - tail_start;
+    const long long per_tail_region = (long long)p.blocks_per_region * (kBM / 4);
+    g = p.tail_region + q / per_tail_region;
+    r = q - (g - p.tail_region) * per_tail_region;
+    per_block = kBM / 4;
+    it.rows = 4;
   }
+  const Region reg = region_at(g, p.mt_count, p.nt_count, p.band);
+  it.block = (reg.mt * p.nt_count + reg.nt) * p.blocks_per_region + (int)(r / per_block);
+  it.part = (int)(r % per_block);
+  return it;
 }
 
-// Take the next FIFO position and wait for its item: the item, -1 when every
-// item of the run is taken, -2 if the wait gave up.  Every lane acquires the
-// filled slot itself, so each lane's loads of the staging are ordered after
-// the releases that completed the block.  *slot_out: the item's FIFO slot.
-__device__ __forceinline__ int queue_pop(const GemmParams& p, int lane,
-                                         unsigned long long** slot_out) {
+// First order position of a block's items, and how many it has (the inverse
+// of item_at; used only to stamp the debug timeline).
+__device__ __forceinline__ long long first_item_of(const GemmParams& p, int block, int* count) {
+  const int phys = block / p.blocks_per_region;
+  const int rb = block - phys * p.blocks_per_region;
+  const int mt = phys / p.nt_count, nt = phys - (phys / p.nt_count) * p.nt_count;
+  const int b = mt / p.band, mt0 = b * p.band;
+  const int h = (p.mt_count - mt0) < p.band ? (p.mt_count - mt0) : p.band;
+  const long long g = (long long)b * p.band * p.nt_count + (long long)nt * h + (mt - mt0);
+  const long long per_region = (long long)p.blocks_per_region * p.splits;
+  if (g < p.tail_region) {
+    *count = p.splits;
+    return g * per_region + (long long)rb * p.splits;
+  }
+  *count = kBM / 4;
+  return (long long)p.tail_region * per_region +
+         (g - p.tail_region) * p.blocks_per_region * (kBM / 4) + (long long)rb * (kBM / 4);
+}
+
+// Take the next item position and wait until its block is complete (all 32
+// release adds of this run): 1 with *it and *pos set, 0 when every item of
+// the run is taken, -1 if the wait gave up.  Lane 0 polls with relaxed loads
+// (an acquire per poll would cost every waiting warp an L1 invalidation); once
+// the count is complete every lane acquires it itself, so each lane's loads of
+// the staging are ordered after the releases that completed the block.
+__device__ __forceinline__ int item_pop(const GemmParams& p, int lane, Item* it, long long* pos_out) {
   uint32_t pos = 0;
   if (lane == 0) pos = atomicAdd(p.ctrl + kCtrlQueueHead * kCtrlStride, 1u);
   pos = __shfl_sync(0xffffffffu, pos, 0);
-  if ((long long)pos >= p.num_items) return -1;
-  const unsigned long long* slot = p.queue + (size_t)pos * kQueueStride;
+  if ((long long)pos >= p.num_items) return 0;
+  *it = item_at(p, pos);
+  *pos_out = pos;
+  const uint32_t* cnt = p.flags + (size_t)it->block * kFlagStride;
   uint64_t t0 = 0;
   if (lane == 0) t0 = globaltimer_ns();
-  uint32_t sleep_ns = 64;
+  uint32_t sleep_ns = 32;
   while (true) {
-    // poll with relaxed loads (an acquire per poll would cost every waiting
-    // warp an L1 invalidation); acquire once the slot is filled
     int ready = 0;
-    if (lane == 0) ready = (uint32_t)(ld_relaxed_gpu_u64(slot) >> 32) == p.epoch;
+    if (lane == 0) ready = (int)(ld_relaxed_gpu(cnt) - p.flag_target) >= 0;
     if (__shfl_sync(0xffffffffu, ready, 0)) {
-      const uint64_t v = ld_acquire_gpu_u64(slot);
-      *slot_out = const_cast<unsigned long long*>(slot);
-      return (int)(uint32_t)v;
+      (void)ld_acquire_gpu(cnt);
+      return 1;
     }
     int give_up = 0;
     if (lane == 0)
       give_up = (globaltimer_ns() - t0 > p.timeout_ns) || ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride);
-    if (__shfl_sync(0xffffffffu, give_up, 0)) return -2;
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return -1;
     __nanosleep(sleep_ns);
-    sleep_ns = sleep_ns < 1024 ? sleep_ns * 2 : 1024;
+    sleep_ns = sleep_ns < 256 ? sleep_ns * 2 : 256;
   }
 }
 
@@ -315,16 +363,14 @@ __device__ __forceinline__ void reduce_rows(const GemmParams& p, size_t plane, i
 // Reduce one item of a completed 128-row block (lane l covers columns
 // [8l, 8l+8) of the block's 256).  With p.staging_in_l2 the staging lines
 // just read are dropped from L2.
-__device__ __forceinline__ void reduce_item(const GemmParams& p, int item, int lane) {
+__device__ __forceinline__ void reduce_item(const GemmParams& p, const Item& it, int lane) {
   const size_t plane = (size_t)p.plane;
-  const int block = item >> 5;
-  const int part = item & 31;
-  const int region = block / p.blocks_per_region;
-  const int rb = block - region * p.blocks_per_region;
+  const int region = it.block / p.blocks_per_region;
+  const int rb = it.block - region * p.blocks_per_region;
   const int mt = region / p.nt_count;
   const int nt = region - mt * p.nt_count;
-  const int rows = region >= p.tail_region ? 4 : p.unit_rows;
-  const int row_begin = mt * p.tile_rows + rb * kBM + part * rows;
+  const int rows = it.rows;
+  const int row_begin = mt * p.tile_rows + rb * kBM + it.part * rows;
   if (row_begin >= p.M) return;  // rows of a ragged last tile that do not exist
   int row_end = row_begin + rows;
   if (row_end > p.M) row_end = p.M;
@@ -398,7 +444,7 @@ __device__ __forceinline__ bool wait_for_share(const GemmParams& p, int my_idx, 
   return __shfl_sync(0xffffffffu, go, 0) != 0;
 }
 
-// Reducer role: take FIFO positions until every item of the run is taken.
+// Reducer role: take item positions until every item of the run is taken.
 // Items done are counted in the CTA's shared counter (added to the run's
 // total once, when the CTA ends).  my_idx: the warp's index among the CTA's
 // reducer warps (-1 for epilogue warps that joined: never held back).
@@ -408,21 +454,24 @@ __device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_
   Controller ctl;
   while (true) {
     if (p.adaptive && my_idx > 0 && !wait_for_share(p, my_idx, lane)) break;
-    unsigned long long* slot = nullptr;
-    const int item = queue_pop(p, lane, &slot);
-    if (item == -1) break;
-    if (item == -2) {
+    Item it;
+    long long pos = 0;
+    const int got = item_pop(p, lane, &it, &pos);
+    if (got == 0) break;
+    if (got < 0) {
       if (lane == 0 && !ld_volatile_u32(p.ctrl + kCtrlAbort * kCtrlStride))
-        record_error(p, kErrFlagTimeout, kWhereReducer, 0xFFFFFFFFu);
+        record_error(p, kErrFlagTimeout, kWhereReducer, (uint32_t)it.block);
       break;
     }
     const long long c0 = controller ? clock64() : 0;
     const uint64_t t_take = (p.trace && lane == 0) ? globaltimer_ns() : 0;
-    reduce_item(p, item, lane);
+    reduce_item(p, it, lane);
     __syncwarp();
     if (lane == 0) atomicAdd(cta_reduced, 1u);
     if (controller) ctl.update(p, clock64() - c0);
-    if (p.trace && lane == 0) {  // debug timeline: taken, done (words 2 and 3 of the slot)
+    if (p.trace && lane == 0) {  // debug timeline: item, taken, done (words 0, 2 and 3)
+      unsigned long long* slot = p.queue + (size_t)pos * kQueueStride;
+      st_relaxed_gpu_u64(slot, ((uint64_t)p.epoch << 32) | (uint32_t)((it.block << 5) | it.part));
       st_relaxed_gpu_u64(slot + 2, t_take);
       st_relaxed_gpu_u64(slot + 3, globaltimer_ns());
     }
@@ -431,15 +480,22 @@ __device__ __noinline__ void reducer_loop(const GemmParams& p, int lane, uint32_
 
 // One epilogue warp's 32 rows of a rank tile are stored (and ordered before
 // this thread by __syncwarp): count them with a release add on the 128-row
-// block's completion count; the add that completes the block acquires the
-// other adds and queues the block's items.
+// block's completion count.  The add returns nothing, so the warp does not
+// wait for a reply; the reducers poll the count.  With the debug timeline the
+// add returns the old count, and the add that completes the block stamps the
+// time its items became ready.
 __device__ __forceinline__ void publish_rows(const GemmParams& p, int block, bool skip) {
   if (skip) return;  // debug: this completion never arrives
-  const uint32_t old = atom_add_release_gpu(p.flags + (size_t)block * kFlagStride, 1u);
-  if (old == p.flag_target - 1u) {
-    fence_acq_rel_gpu();  // acquire the other warps' releases, release to the FIFO
-    const int region = block / p.blocks_per_region;
-    queue_push_block(p, block, region >= p.tail_region ? kBM / 4 : p.splits);
+  uint32_t* cnt = p.flags + (size_t)block * kFlagStride;
+  if (!p.trace) {
+    red_release_gpu_add(cnt, 1u);
+    return;
+  }
+  if (atom_add_release_gpu(cnt, 1u) == p.flag_target - 1u) {
+    int n = 0;
+    const long long first = first_item_of(p, block, &n);
+    const uint64_t now = globaltimer_ns();
+    for (int i = 0; i < n; ++i) st_relaxed_gpu_u64(p.queue + (size_t)(first + i) * kQueueStride + 1, now);
   }
 }
 
@@ -617,7 +673,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
                                   1) gemm_rs_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool kFused = kKind == kKindRS;  // reduce-scatter (or all-reduce) fused
   constexpr bool kAG = kKind == kKindAG;     // all-gather fused
-  using C = TileCfg<kCtas>;
+  using C = TileCfg<kKind, kCtas>;
   using Ring = TileRing<kCtas>;
   constexpr int kPair = C::kPair;
   extern __shared__ uint8_t smem_raw[];
