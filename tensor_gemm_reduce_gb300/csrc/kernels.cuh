@@ -296,10 +296,11 @@ __device__ __forceinline__ long long first_item_of(const GemmParams& p, int bloc
 
 // Take the next item position and wait until its block is complete (all 32
 // release adds of this run): 1 with *it and *pos set, 0 when every item of
-// the run is taken, -1 if the wait gave up.  Lane 0 polls with relaxed loads
-// (an acquire per poll would cost every waiting warp an L1 invalidation); once
-// the count is complete every lane acquires it itself, so each lane's loads of
-// the staging are ordered after the releases that completed the block.
+// the run is taken, -1 if the wait gave up.  Lane 0 polls with acquire loads
+// (the reducers read the staging through L2 only, so the L1 invalidation of
+// an acquire costs nothing); the warp barrier after the successful poll
+// orders every lane's staging loads after lane 0's acquire, and so after the
+// releases that completed the block.
 __device__ __forceinline__ int item_pop(const GemmParams& p, int lane, Item* it, long long* pos_out) {
   uint32_t pos = 0;
   if (lane == 0) pos = atomicAdd(p.ctrl + kCtrlQueueHead * kCtrlStride, 1u);
@@ -313,9 +314,9 @@ __device__ __forceinline__ int item_pop(const GemmParams& p, int lane, Item* it,
   uint32_t sleep_ns = 32;
   while (true) {
     int ready = 0;
-    if (lane == 0) ready = (int)(ld_relaxed_gpu(cnt) - p.flag_target) >= 0;
+    if (lane == 0) ready = (int)(ld_acquire_gpu(cnt) - p.flag_target) >= 0;
     if (__shfl_sync(0xffffffffu, ready, 0)) {
-      (void)ld_acquire_gpu(cnt);
+      __syncwarp();
       return 1;
     }
     int give_up = 0;
