@@ -63,6 +63,9 @@ def parse_args(argv=None):
                         "all-gather shape) timed per shape instead of the benchmark line; for "
                         "all-gather shapes t_rs is the gather alone")
     p.add_argument("--sweep-rounds", type=int, default=3)
+    p.add_argument("--tuned", action="store_true",
+                   help="--sweep: also run the auto-tuner (gemm_rs_tune, FUSED) on each shape and time "
+                        "its plan beside the default one")
     p.add_argument("--sweep-iters", type=int, default=0, help="timed launches per mode and round (0: auto)")
     p.add_argument("--ag-workload", default="llama3_70b_qkv_m2048",
                    help="all-gather + GEMM workload timed beside the main one ('' to skip)")
@@ -347,6 +350,16 @@ def run_ours(args, rank, world, local):
     t_fused = time_mode(G.FUSED, it, 20)
     t_unfused = time_mode(G.UNFUSED, it, 20)
     eff = metrics.overlap_efficiency(t_gemm, t_rs, t_fused)
+    # The same fused run with the staging forced through HBM: staging stores
+    # without the L2 evict-last hint and no discard after reduction, so the
+    # partials are written back to DRAM as a peer write over a link would be
+    # (the GEMM-alone run, T_gemm, writes its staging the same way).
+    hplan = G.Plan(M, N, K, debug_flags=G.DEBUG_NO_STAGING_L2)
+    ws_h = hplan.new_workspace()
+    t_fused_hbm = time_mode(G.FUSED, it, 20, hplan, ws_h)
+    hplan.close()
+    del ws_h
+    eff_hbm = metrics.overlap_efficiency(t_gemm, t_rs, t_fused_hbm)
 
     # the prior stream-overlap method (row chunks, reduce of chunk c beside the
     # GEMM of chunk c+1 on a second stream), on a workspace of its own
@@ -525,6 +538,7 @@ def run_ours(args, rank, world, local):
                    "unit_rows": info.unit_rows},
         "overlap": {"efficiency": eff, "t_gemm_us": t_gemm * 1e6, "t_rs_us": t_rs * 1e6,
                     "t_fused_us": t_fused * 1e6, "t_unfused_us": t_unfused * 1e6,
+                    "efficiency_staging_hbm": eff_hbm, "t_fused_staging_hbm_us": t_fused_hbm * 1e6,
                     "fused_speedup_vs_unfused": t_unfused / t_fused, "iters": it,
                     "t_chunked_us": {c: t * 1e6 for c, t in t_chunked.items()},
                     "fused_speedup_vs_best_chunked":
@@ -630,13 +644,38 @@ def run_sweep(args, local):
         if plan.status() != G.GEMM_RS_OK:
             raise RuntimeError(f"{name}: device status")
         t = {k: metrics.median(v) for k, v in times.items()}
+        tuned = None
+        if args.tuned:
+            op = G.OP_AG if w.op == "ag" else G.OP_RS
+            best, best_us, table = G.tune(w.M, w.N, w.K, A, W, out, mode=G.FUSED, iters=iters,
+                                          rounds=args.sweep_rounds, op=op)
+            tplan = G.Plan(w.M, w.N, w.K, **{k: v for k, v in best.items() if k != "timeout_ns"})
+            tws = tplan.new_workspace()
+            tplan.run(A, W, out, tws, G.FUSED)
+            torch.cuda.synchronize()
+            if tplan.status() != G.GEMM_RS_OK or not torch.equal(ref.view(torch.int16), out.view(torch.int16)):
+                raise RuntimeError(f"{name}: the tuned plan's output differs")
+            tt = []
+            for _ in range(args.sweep_rounds):  # interleaved with the default plan again
+                for pl, wsx, key in ((plan, ws, "default"), (tplan, tws, "tuned")):
+                    for _ in range(2):
+                        pl.run(A, W, out, wsx, G.FUSED)
+                    tt.append((key, time_batched(lambda: pl.run(A, W, out, wsx, G.FUSED), iters, 1, stream)))
+            t_def = metrics.median([v for k, v in tt if k == "default"])
+            t_tun = metrics.median([v for k, v in tt if k == "tuned"])
+            knobs = {k: best[k] for k in ("mma_ctas", "reducer_warps", "unit_rows", "band_m", "tail_waves")}
+            tuned = {"plan": knobs, "t_fused_tuned_us": t_tun * 1e6, "t_fused_default_us": t_def * 1e6,
+                     "tuner_best_us": best_us, "candidates": len(table)}
+            tplan.close()
+            del tws
         print(json.dumps({
             "sweep": name, "layer": "all-gather + GEMM" if w.op == "ag" else "GEMM + reduce-scatter",
             "M": w.M, "N": w.N, "K": w.K,
             "tflops_fused": w.flops / t["fused"] / 1e12, "tflops_gemm": w.flops / t["gemm"] / 1e12,
             "overlap_efficiency": metrics.overlap_efficiency(t["gemm"], t["rs"], t["fused"]),
             "fused_speedup_vs_unfused": t["unfused"] / t["fused"],
-            **{f"t_{k}_us": v * 1e6 for k, v in t.items()}, "iters": args.sweep_rounds * iters}),
+            **{f"t_{k}_us": v * 1e6 for k, v in t.items()}, "iters": args.sweep_rounds * iters,
+            "tuned": tuned}),
             flush=True)
         plan.close()
         del A, W, out, ws, ref

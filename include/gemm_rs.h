@@ -125,7 +125,7 @@ typedef struct gemm_rs_desc {
   int32_t world;          /* tensor-parallel degree; must be 8 */
   int64_t M, N, K;        /* M%8 == 0, N%8 == 0, K%64 == 0 (so K/8 is a multiple of 8); 0 allowed */
   int32_t reducer_warps;  /* FUSED: reducer warps per CTA (all-gather: copy warps), 1..6;
-                             0 = default (4; all-gather 2) */
+                             0 = default (4, or 2 when K >= 16384; all-gather 2) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
   int32_t unit_rows;      /* rows per reduce item in FUSED mode: 4, 8, 16 or 32; 0 = 8 */
@@ -291,22 +291,27 @@ int gemm_rs_destroy(gemm_rs_t plan);
 /*
  * Auto-tuning (FLUX page, TL;DR: tile swizzling and auto-tuning; mKernel page,
  * section 5.5: the best share of communication workers varies with the kernel
- * and the shape).  The candidates for d's problem are d with, in turn:
- *   reduce-scatter / all-reduce: mma_ctas in {2, 1} x reducer_warps in {2, 4, 6}
- *     x unit_rows in {8, 16};
- *   all-gather: mma_ctas in {2, 1} x copy warps (reducer_warps) in {1, 2, 4};
- * every other field as in d.  gemm_rs_tune_candidates writes up to `max` of them
- * to `cands` (may be NULL), sets *count, and *workspace_bytes (may be NULL) to
- * the largest workspace any of them needs.  Host only; checks d first.
+ * and the shape).  The candidates for d's problem are, without duplicates:
+ *   d itself (first);
+ *   d with mma_ctas in {2, 1} x reducer_warps in {2, 4, 6} x unit_rows in
+ *     {8, 16} (all-gather: mma_ctas in {2, 1} x copy warps in {1, 2, 4});
+ *   d with band_m (the tile-order swizzle band) at 1/2 and 1/4 of the
+ *     automatic band;
+ *   reduce-scatter: d with tail_waves in {1, 2, 6};
+ * every other field as in d (zeros stand for the defaults).  gemm_rs_tune_candidates
+ * writes up to `max` of them to `cands` (may be NULL), sets *count, and
+ * *workspace_bytes (may be NULL) to the largest workspace any of them needs.
+ * Host only; checks d first.
  */
-#define GEMM_RS_TUNE_MAX 16
+#define GEMM_RS_TUNE_MAX 32
 int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max, int* count,
                             size_t* workspace_bytes);
 
 /*
  * Time every candidate of gemm_rs_tune_candidates in `mode` on the caller's
  * buffers (as gemm_rs_run; ws of ws_bytes >= the candidates' largest
- * workspace) and return the fastest in *best with its time in *best_us.
+ * workspace) and return the fastest in *best with its time in *best_us; the
+ * requested plan (candidate 0) is kept unless another beats it by over 1%.
  * Each candidate runs 3 warm-up launches, then `rounds` rounds in which every
  * candidate is timed over `iters` back-to-back runs with CUDA events on
  * `stream` (interleaved, so drifting clocks affect all alike); a candidate's

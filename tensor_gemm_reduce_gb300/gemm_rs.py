@@ -417,7 +417,7 @@ def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Pl
 # auto-tuning
 # ----------------------------------------------------------------------------
 
-TUNE_MAX = 16
+TUNE_MAX = 32
 _DESC_KW = ("reducer_warps", "grid", "band_m", "unit_rows", "timeout_ns", "debug_flags",
             "mma_ctas", "chunks", "replicas", "op", "adaptive", "tail_waves")
 

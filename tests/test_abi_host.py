@@ -165,13 +165,24 @@ def test_ag_schedule_walks_from_own_shard(lib, M, N, K, ctas):
 
 @pytest.mark.parametrize("op", [0, 1])
 def test_tune_candidates_and_their_workspace(lib, op):
-    """The tuner's candidate set (host only): the requested plan with the tile
-    shape and the number of communication warps (and unit rows) varied, and one
-    workspace size that fits every candidate."""
+    """The tuner's candidate set (host only): the requested plan first, then
+    the tile shape and the number of communication warps (and unit rows)
+    varied, narrower tile-order bands and (reduce-scatter) tail waves; no plan
+    twice; one workspace size that fits every candidate."""
     d = G._desc(1024, 2048, 4096, op=op, timeout_ns=7)
     cands, ws = G.tune_candidates(d)
-    assert len(cands) == (12 if op == 0 else 6)
-    assert len({(c.mma_ctas, c.reducer_warps, c.unit_rows) for c in cands}) == len(cands)
+    # auto band at M=1024, K=4096, 256-row tiles: 32 MiB / (256*4096*2) = 16 -> 4 tile rows
+    assert len(cands) == (1 + 11 + 2 + 3 if op == 0 else 1 + 5 + 2)
+    c0 = cands[0]
+    assert (c0.mma_ctas, c0.reducer_warps, c0.unit_rows, c0.band_m, c0.tail_waves) == (0, 0, 0, 0, 0)
+    def resolved(c):
+        return (c.mma_ctas or 2, c.reducer_warps or (4 if op == 0 else 2),  # K = 4096 < 16384
+                (c.unit_rows or 8) if op == 0 else 0, c.band_m or (4 if (c.mma_ctas or 2) == 2 else 8),
+                (c.tail_waves or 3) if op == 0 else 0)
+    assert len({resolved(c) for c in cands}) == len(cands)
+    assert {c.band_m for c in cands} >= {0, 1, 2}
+    if op == 0:
+        assert {c.tail_waves for c in cands} >= {0, 1, 2, 6}
     assert all(c.M == 1024 and c.N == 2048 and c.K == 4096 and c.op == op and c.timeout_ns == 7
                for c in cands)
     staging = 8 * 1024 * (2048 if op == 0 else 4096) * 2

@@ -324,7 +324,10 @@ def test_tuner_picks_a_working_candidate(op):
     ref = out.clone()
     best, best_us, table = G.tune(M, N, K, Ad, Wd, out, mode=G.FUSED, iters=3, rounds=3, op=op)
     assert best_us > 0 and all(t > 0 for _, t in table)
-    assert best_us == min(t for _, t in table)
+    # the fastest candidate, or the requested plan (candidate 0) when nothing
+    # beats it by more than 1%
+    fastest = min(t for _, t in table)
+    assert best_us == fastest or (best_us == table[0][1] and fastest > 0.99 * best_us)
     p = G.Plan(M, N, K, **{k: v for k, v in best.items() if k not in ("timeout_ns",)})
     ws2 = p.new_workspace()
     out.fill_(0)
