@@ -702,6 +702,9 @@ static int run_chunked(gemm_rs_t h, const void* A, void* out, void* ws, cudaStre
                   kWorld, Kr * 2, Kr * 2 * (uint64_t)d.M, kBK, kBM))
       return GEMM_RS_ERR_CUDA;
     p.stage = reinterpret_cast<uint16_t*>(wsb) + row0 * d.N;  // rank planes stay M * N apart
+    if (!make_map(&p.tmap_s, p.stage, (uint64_t)d.N, (uint64_t)rows, kWorld, (uint64_t)d.N * 2,
+                  (uint64_t)d.N * 2 * (uint64_t)d.M, 64, 32))
+      return GEMM_RS_ERR_CUDA;
     p.M = (int)rows;
     p.mt_count = (int)((rows + h->tile_rows - 1) / h->tile_rows);
     p.num_tiles = (long long)kWorld * p.mt_count * h->nt;
@@ -786,6 +789,8 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
                         make_map(&p.tmap_g, wsb, K, M, kWorld, K * 2, K * 2 * M, kBK, kBM)
                   : make_map(&p.tmap_a, wsb, K, M, kWorld, K * 2, K * 2 * M, kBK, kBM);
   ok = ok && make_map(&p.tmap_b, W, cols, K, kWorld, cols * 2, cols * 2 * K, 64, kBK);
+  // epilogue stores into the output [8][M][N/8]: 32 x 64 boxes
+  ok = ok && make_map(&p.tmap_s, out, cols, M, kWorld, cols * 2, cols * 2 * M, 64, 32);
   if (!ok) return GEMM_RS_ERR_CUDA;
   p.stage = static_cast<uint16_t*>(out);  // the epilogue writes C_r = rank r's plane
   p.plane = (long long)(M * cols);
@@ -891,6 +896,10 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
                     (uint64_t)d.N * 2 * Kr, 64, kBK))
         return GEMM_RS_ERR_CUDA;
     }
+    // epilogue stores into the staging: 32 x 64 boxes
+    if (!make_map(&p.tmap_s, wsb, (uint64_t)d.N, (uint64_t)d.M, kWorld, (uint64_t)d.N * 2,
+                  (uint64_t)d.N * 2 * (uint64_t)d.M, 64, 32))
+      return GEMM_RS_ERR_CUDA;
     p.stage = reinterpret_cast<uint16_t*>(wsb);
     p.plane = d.M * d.N;
     p.replicas = replicas_of(&d);
@@ -1140,6 +1149,9 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     if (!make_map(&p.tmap_a, A, Kr, (uint64_t)M, kWorld, Kr * 2, Kr * 2 * (uint64_t)M, kBK, kBM) ||
         !make_map(&p.tmap_b, W, (uint64_t)N, Kr, kWorld, (uint64_t)N * 2, (uint64_t)N * 2 * Kr, 64,
                   kBK))
+      return GEMM_RS_ERR_CUDA;
+    if (!make_map(&p.tmap_s, scratch, (uint64_t)N, (uint64_t)M, kWorld, (uint64_t)N * 2,
+                  (uint64_t)N * 2 * (uint64_t)M, 64, 32))
       return GEMM_RS_ERR_CUDA;
     p.stage = reinterpret_cast<uint16_t*>(scratch);
     p.staging_in_l2 = (N % 64 == 0);  // as a default plan: the array is 256-byte aligned

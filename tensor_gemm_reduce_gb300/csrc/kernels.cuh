@@ -21,10 +21,10 @@
 //   warp 1        MMA issuer (the pair's first CTA only): tcgen05.mma
 //                 (bf16 in, fp32 in TMEM, two 256-column accumulators);
 //                 TMEM allocation in every CTA
-//   warps 2..5    epilogue: TMEM -> registers -> bf16 (RNE) -> an 8 x 8
-//                 transpose of 16-byte granules inside each 8-lane group ->
-//                 coalesced stores into the rank's staging region (every store
-//                 instruction writes four whole 128-byte row segments); then
+//   warps 2..5    epilogue: TMEM -> registers (one row per lane) -> bf16
+//                 (RNE) -> the warp's 32 x 64 block written into a shared
+//                 buffer in the 128-byte swizzle -> one TMA store of the
+//                 block into the rank's staging region; then
 //                 (fused kernel) each warp publishes its 32 rows with a release
 //                 add on the 128-row block's completion count (8 ranks x 4
 //                 warps = 32 adds per block and run)
@@ -58,20 +58,23 @@ constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
 constexpr int kMaxReducerWarps = 6;
 
+// Epilogue buffers: each epilogue warp stages 32 rows x 64 columns of bf16
+// (4 KiB, 128-byte swizzle) in shared memory for a TMA store, two buffers
+// per warp so one can fill while the other's store reads it.
+constexpr int kEpiBufBytes = 32 * 64 * 2;
+constexpr int kEpiSmem = kEpiWarps * 2 * kEpiBufBytes;
+
 // Shared-memory plan of one CTA.  kCtas = CTAs of the cluster that share a
 // tile: 1 (one-CTA MMA) or 2 (one 2-CTA MMA).  Every CTA loads its own
-// operands; no load is shared between CTAs.
-// The epilogue needs no shared memory, so the operand stages may take all of
-// it but the barriers.  The GEMM alone and the all-gather use 7 stages; the
-// fused reduce-scatter uses 6: every stage in flight also queues in front of
-// the reducers' loads and the epilogue's stores in the memory system, and
-// with 6 the fused run is faster (o_proj 206 -> 203 us, 2048 x 6144 x 6144
-// 143 -> 139 us) while the GEMM alone loses about 1%.
+// operands; no load is shared between CTAs.  6 operand stages of 32 KiB (4 of
+// 48 KiB with one CTA) and 32 KiB of epilogue buffers.  Fewer stages in
+// flight also queue less in front of the reducers' loads (fused o_proj: 7
+// stages 206 us, 6 stages 203 us).
 template <int kKind, int kCtas>
 struct TileCfg {
   static_assert(kCtas == 1 || kCtas == 2, "one CTA or a CTA pair per tile");
   static constexpr int kPair = kCtas;                  // CTAs per MMA
-  static constexpr int kStages = kCtas == 1 ? 4 : (kKind == kKindRS ? 6 : 7);
+  static constexpr int kStages = kCtas == 1 ? 4 : 6;
   static constexpr int kTileRows = kBM * kCtas;        // output rows of one cluster tile
   static constexpr int kBCols = kBN / kPair;           // W columns held by one CTA
   static constexpr int kBBoxes = kBCols / 64;          // 64-column TMA boxes per stage
@@ -81,7 +84,8 @@ struct TileCfg {
   static constexpr int kStage = kAStage + kBStage;     // bytes one CTA loads per stage
   static constexpr int kSmemA = 0;
   static constexpr int kSmemB = kSmemA + kStages * kAStage;
-  static constexpr int kSmemBar = kSmemB + kStages * kBStage;
+  static constexpr int kSmemEpi = kSmemB + kStages * kBStage;  // 1024-byte aligned
+  static constexpr int kSmemBar = kSmemEpi + kEpiSmem;
   // full[S], empty[S], acc_full[2], acc_empty[2], drain, tile ring full[4], empty[4]
   static constexpr int kNumBars = 2 * kStages + 5 + 2 * 4;
   static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
@@ -120,6 +124,9 @@ enum ErrWhere : uint32_t {
 struct GemmParams {
   CUtensorMap tmap_a;   // A  [8][M][Kr] : dims {Kr, M, 8}, box {64, 128, 1}
   CUtensorMap tmap_b;   // W  [8][Kr][N] : dims {N, Kr, 8}, box {64, 64, 1}
+  // Epilogue stores: the staging [8][M][N] (all-gather: the output
+  // [8][M][N/8]) : dims {N, M, 8}, box {64, 32, 1}, 128-byte swizzle.
+  CUtensorMap tmap_s;
   // All-gather + GEMM (kKindAG): tmap_a covers the input's row shards
   // [8][M/8][K] (dims {K, M/8, 8}), tmap_g the gather buffers [8][M][K]
   // (dims {K, M, 8}; rank r's copy of every shard).  Kr is then the full K and
@@ -497,32 +504,6 @@ __device__ __forceinline__ void publish_rows(const GemmParams& p, int block, boo
     const long long first = first_item_of(p, block, &n);
     const uint64_t now = globaltimer_ns();
     for (int i = 0; i < n; ++i) st_relaxed_gpu_u64(p.queue + (size_t)(first + i) * kQueueStride + 1, now);
-  }
-}
-
-// Transpose 8 x 8 granules of 16 bytes across the 8 lanes of a group (t =
-// lane & 7): before, x[j] is granule j of the lane's own row; after, x[j] is
-// granule t of the group's row j.  Three butterfly steps; in step m a lane
-// swaps with lane t ^ m the half of its granules whose index differs from t in
-// bit m.
-__device__ __forceinline__ void transpose_granules(uint32_t (&x)[8][4], int t) {
-#pragma unroll
-  for (int s = 0; s < 3; ++s) {
-    const int m = 4 >> s;
-    const bool upper = (t & m) != 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & m) continue;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t send = upper ? x[j][k] : x[j | m][k];
-        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
-        if (upper)
-          x[j][k] = recv;
-        else
-          x[j | m][k] = recv;
-      }
-    }
   }
 }
 
@@ -916,11 +897,15 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;     // TMEM lane quadrant this warp can read
     const int ew = warp - 2;
-    const int t8 = lane & 7;    // granule this lane stores after the transpose
-    const int grp = lane & 24;  // first row of the lane's 8-row group
     const bool hint = kFused && p.staging_in_l2;
     const uint64_t keep_policy = hint ? policy_evict_last() : 0;
-    int acc = 0;
+    // this warp's two shared buffers; lane l writes row l of a 32 x 64 block,
+    // its 16-byte granule j at position j ^ (l % 8) (the 128-byte swizzle the
+    // store's tensor map expects), so a warp's 16-byte writes fill 4 whole
+    // 128-byte shared-memory wavefronts
+    const uint32_t ebuf = sbase + C::kSmemEpi + (uint32_t)ew * 2 * kEpiBufBytes;
+    const uint32_t lane_row = ebuf + (uint32_t)lane * 128;
+    int acc = 0, nbuf = 0;
     uint32_t acc_phase = 0;
     while (true) {
       int idx = -1, got = 0;
@@ -942,8 +927,7 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
       if (idx < 0) break;
       const TileCoord tc = coord(idx);
       tc_fence_after();
-      const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32 + grp;
-      uint16_t* stage_r = p.stage + (size_t)tc.rank * (size_t)p.plane;
+      const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32;  // the warp's first row
 #pragma unroll 1
       for (int c = 0; c < kBN / 64; ++c) {
         uint32_t v0[32], v1[32];
@@ -964,34 +948,39 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
               mbar_arrive_remote(mapa_shared(bar_acc_empty + 8 * acc, mma_leader_rank));
           }
         }
-        // granule j = the 8 columns [8j, 8j + 8) of this chunk of the lane's row
-        uint32_t x[8][4];
+        const int col = tc.nt * kBN + c * 64;
+        if (row0 < p.M && col < p.N) {  // warp-uniform; the store clips ragged edges
+          const uint32_t buf = lane_row + (uint32_t)nbuf * kEpiBufBytes;
+          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            x[j][k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-        }
-        transpose_granules(x, t8);
-        const int col = tc.nt * kBN + c * 64 + 8 * t8;
-        if (col < p.N) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (row0 + j < p.M) {
-              uint16_t* dst = stage_r + (size_t)(row0 + j) * p.N + col;
-              const uint4 w = make_uint4(x[j][0], x[j][1], x[j][2], x[j][3]);
-              if (hint)
-                st_global_v4_hint(dst, w, keep_policy);
-              else
-                st_global_v4(dst, w);
-            }
+          for (int j = 0; j < 8; ++j) {  // granule j = columns [8j, 8j + 8) of the lane's row
+            const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
+            st_shared_v4(buf + (uint32_t)((j ^ (lane & 7)) << 4),
+                         pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                         pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                         pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                         pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
           }
+          fence_proxy_async_shared();  // the writes, before the async proxy reads them
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t block_src = ebuf + (uint32_t)nbuf * kEpiBufBytes;
+            if (hint)
+              tma_store_3d_hint(&p.tmap_s, block_src, col, row0, tc.rank, keep_policy);
+            else
+              tma_store_3d(&p.tmap_s, block_src, col, row0, tc.rank);
+            bulk_commit_group();
+          }
+          nbuf ^= 1;
         }
       }
       if (kFused) {
-        __syncwarp();  // the warp's stores are ordered before lane 0's release
         if (lane == 0) {
+          // the warp's rows of this tile are in the staging (async proxy),
+          // ordered before the release that publishes them
+          bulk_wait_group<0>();
+          fence_proxy_async_global();
           const int block =
               ((int)(tc.mt * p.nt_count + tc.nt)) * p.blocks_per_region + (int)cta_rank;
           publish_rows(p, block, (p.debug_flags & 1u) && idx == 0 && first_cta && ew == 0);
@@ -1001,6 +990,8 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_group<0>();  // the last stores have read their buffers and landed
+    __syncwarp();
     if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
     if (kFused) reducer_loop(p, lane, cta_reduced, -1);  // out of tiles: help with the reduction
   } else {
