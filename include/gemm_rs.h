@@ -124,7 +124,7 @@ enum gemm_rs_mode {
 typedef struct gemm_rs_desc {
   int32_t world;          /* tensor-parallel degree; must be 8 */
   int64_t M, N, K;        /* M%8 == 0, N%8 == 0, K%64 == 0 (so K/8 is a multiple of 8); 0 allowed */
-  int32_t reducer_warps;  /* FUSED: reducer warps per CTA (all-gather: copy warps), 1..6;
+  int32_t reducer_warps;  /* FUSED: reducer warps per CTA (all-gather: copy warps), 1..5;
                              0 = default (4, or 2 when K >= 16384; all-gather 2) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
@@ -293,7 +293,7 @@ int gemm_rs_destroy(gemm_rs_t plan);
  * section 5.5: the best share of communication workers varies with the kernel
  * and the shape).  The candidates for d's problem are, without duplicates:
  *   d itself (first);
- *   d with mma_ctas in {2, 1} x reducer_warps in {2, 4, 6} x unit_rows in
+ *   d with mma_ctas in {2, 1} x reducer_warps in {2, 4, 5} x unit_rows in
  *     {8, 16} (all-gather: mma_ctas in {2, 1} x copy warps in {1, 2, 4});
  *   d with band_m (the tile-order swizzle band) at 1/2 and 1/4 of the
  *     automatic band;

@@ -357,7 +357,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
                                                      : kDefaultReducerWarps;
   int grid = 0;
   rc = prepare_kernels(dev, prop.multiProcessorCount, pair, d->grid,
-                       32 * (kGemmWarps + reducer_warps), &grid);
+                       32 * cta_warps(reducer_warps), &grid);
   if (rc) return rc;
 
   gemm_rs_plan_s* h = new (std::nothrow) gemm_rs_plan_s();
@@ -424,7 +424,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   memset(info, 0, sizeof(*info));
   info->num_sms = h->num_sms;
   info->grid = h->grid;
-  info->threads_fused = 32 * (kGemmWarps + h->reducer_warps);
+  info->threads_fused = 32 * cta_warps(h->reducer_warps);
   info->threads_gemm = 32 * kGemmWarps;
   info->smem_bytes = gemm_smem_max(h->pair);
   info->band_m = h->band;
@@ -496,7 +496,7 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
   // the requested plan first, then tile shape x communication warps (x item rows)
   add({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, d->tail_waves});
   static const int kCtas[2] = {2, 1};
-  static const int kWarpsRs[3] = {2, 4, 6}, kWarpsAg[3] = {1, 2, 4};
+  static const int kWarpsRs[3] = {2, 4, 5}, kWarpsAg[3] = {1, 2, 4};
   static const int kUnits[2] = {8, 16};
   for (int c = 0; c < 2; ++c)
     for (int w = 0; w < 3; ++w)
@@ -648,7 +648,7 @@ int gemm_rs_destroy(gemm_rs_t h) {
 
 static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
   return launch_gemm_kernel(h->pair, fused ? kKindRS : kKindGemm, h->grid,
-                            32 * (kGemmWarps + (fused ? h->reducer_warps : 0)), h->params, st);
+                            32 * (fused ? cta_warps(h->reducer_warps) : kGemmWarps), h->params, st);
 }
 
 // Reduce kernel over output rows [row0, row0 + rows).
@@ -834,7 +834,7 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
   if (fused) {
     h->epoch += 1;
     p.ag_target = (uint32_t)h->chunks_per_shard * h->epoch;  // every copied (rank, shard)
-    return launch_gemm_kernel(h->pair, kKindAG, h->grid, 32 * (kGemmWarps + h->reducer_warps),
+    return launch_gemm_kernel(h->pair, kKindAG, h->grid, 32 * cta_warps(h->reducer_warps),
                               p, st);
   }
   if (mode == GEMM_RS_UNFUSED) {
@@ -1085,7 +1085,7 @@ int noalloc_setup(int dev, const NoallocDevice** out) {
     }
     int grid = 0;
     const int rc = prepare_kernels(dev, sms, kDefaultMmaCtas, 0,
-                                   32 * (kGemmWarps + kDefaultReducerWarps), &grid);
+                                   32 * cta_warps(kDefaultReducerWarps), &grid);
     if (rc != GEMM_RS_OK) return rc;
     d.scratch = static_cast<uint8_t*>(p);
     d.num_sms = sms;
@@ -1183,7 +1183,7 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.flag_target = (uint32_t)(kWorld * kEpiWarps);  // counts were just cleared: one run's adds
     p.timeout_ns = kDefaultTimeoutNs;
     rc = launch_gemm_kernel(kDefaultMmaCtas, kKindRS, nd->grid,
-                            32 * (kGemmWarps + kDefaultReducerWarps), p, st);
+                            32 * cta_warps(kDefaultReducerWarps), p, st);
     if (rc != GEMM_RS_OK) return rc;
   }
   if (error_word && cudaMemcpyAsync(error_word, ctrl + kCtrlError * kCtrlStride, sizeof(uint32_t),

@@ -56,7 +56,17 @@ enum Kind : int {
 constexpr int kEpiWarps = 4;
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
-constexpr int kMaxReducerWarps = 6;
+constexpr int kMaxReducerWarps = 5;
+
+// Communication warps (reducers or copy warps) follow the GEMM warps, except
+// that warp 9 is left idle once there are 4 or more of them: warp w runs on
+// the SM sub-partition w % 4, and a reducer beside the MMA warp (warp 1) slows
+// the MMA stream it shares issue slots with (no-load fused runs: 167 cycles per
+// 256x256x16 MMA with a reducer on that sub-partition, 153 without).
+__host__ __device__ constexpr int cta_warps(int comm_warps) {
+  return kGemmWarps + comm_warps + (comm_warps >= 4 ? 1 : 0);
+}
+constexpr int kSkippedWarp = kGemmWarps + 3;  // on the MMA warp's sub-partition
 
 // Epilogue buffers: each epilogue warp stages 32 rows x 64 columns of bf16
 // (4 KiB, 128-byte swizzle) in shared memory for a TMA store, two buffers
@@ -651,7 +661,7 @@ struct TileRing {
 // The persistent GEMM kernel.  kKind adds the fused communication role (see
 // Kind); kCtas selects the tile shape (see TileCfg).
 template <int kKind, int kCtas>
-__global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : kMaxReducerWarps)),
+__global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_warps(kMaxReducerWarps)),
                                   1) gemm_rs_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool kFused = kKind == kKindRS;  // reduce-scatter (or all-reduce) fused
   constexpr bool kAG = kKind == kKindAG;     // all-gather fused
@@ -994,9 +1004,10 @@ __global__ void __launch_bounds__(32 * (kGemmWarps + (kKind == kKindGemm ? 0 : k
     __syncwarp();
     if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
     if (kFused) reducer_loop(p, lane, cta_reduced, -1);  // out of tiles: help with the reduction
-  } else {
+  } else if (!(warp == kSkippedWarp && (int)(blockDim.x >> 5) - kGemmWarps >= 5)) {
     // ------------------------------------------------- reducers / copy warps
-    if (kFused) reducer_loop(p, lane, cta_reduced, warp - kGemmWarps);
+    const int comm_idx = warp - kGemmWarps - (warp > kSkippedWarp ? 1 : 0);
+    if (kFused) reducer_loop(p, lane, cta_reduced, comm_idx);
     if (kAG) copy_loop(p, lane);
   }
 

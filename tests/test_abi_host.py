@@ -49,7 +49,7 @@ def _create(**kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(world=4), G.GEMM_RS_ERR_INVALID_ARG),
-    (dict(reducer_warps=7), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(reducer_warps=6), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(reducer_warps=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(unit_rows=12), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(unit_rows=64), G.GEMM_RS_ERR_INVALID_ARG),

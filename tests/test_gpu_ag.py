@@ -90,7 +90,7 @@ def test_tiny_workload():
     (392, 1536, 1600, {}, False),                  # ragged M and K; 49-row shards
     (8, 512, 64, {}, False),                       # one row per shard
     (2048, 2560, 1024, dict(reducer_warps=1, grid=6), True),  # one copy warp, few CTAs
-    (2048, 2560, 1024, dict(reducer_warps=6), True),
+    (2048, 2560, 1024, dict(reducer_warps=5), True),
     (2048, 4096, 512, dict(grid=8), True),   # 16 tiles per rank >= 2 waves of 4 clusters: paced copies
     (1024, 4096, 512, dict(grid=4, mma_ctas=1), True),  # paced, 1-CTA tiles
 ])

@@ -60,7 +60,7 @@ def test_ragged_and_small_shapes(M, N, K):
     _full_check(A, W, mma_ctas=1)
 
 
-@pytest.mark.parametrize("kw", [dict(reducer_warps=1), dict(reducer_warps=6), dict(grid=3),
+@pytest.mark.parametrize("kw", [dict(reducer_warps=1), dict(reducer_warps=5), dict(grid=3),
                                 dict(band_m=1), dict(unit_rows=8), dict(unit_rows=16), dict(unit_rows=32),
                                 dict(grid=1, reducer_warps=2),
                                 dict(debug_flags=G.DEBUG_NO_STAGING_L2),
@@ -68,7 +68,7 @@ def test_ragged_and_small_shapes(M, N, K):
                                 dict(mma_ctas=1, unit_rows=8, reducer_warps=1),
                                 dict(mma_ctas=2, band_m=1, unit_rows=32),
                                 dict(grid=8, reducer_warps=2),
-                                dict(adaptive=1), dict(adaptive=1, reducer_warps=6, unit_rows=8),
+                                dict(adaptive=1), dict(adaptive=1, reducer_warps=5, unit_rows=8),
                                 dict(adaptive=1, mma_ctas=1, grid=5),
                                 dict(unit_rows=4, tail_waves=1), dict(unit_rows=16, tail_waves=64)])
 def test_plan_variants(kw):
