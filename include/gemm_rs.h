@@ -148,6 +148,11 @@ typedef struct gemm_rs_desc {
                              waves of tiles are reduced in 4-row items (fine grain where the
                              reduction is the critical path), the others in unit_rows-row
                              items; 0 = default (3), 1..64 */
+  int32_t half_regions;   /* row-parallel layer, 2-CTA tiles: the last half_regions regions of
+                             the tile order are computed in half-width tiles (256 rows x 128
+                             columns), so the final wave is shorter; 0 or -1 = none (the
+                             default), 1..4096 (clamped to the regions there are).  Every mode
+                             uses the same tiles, and the results do not depend on it */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -176,6 +181,8 @@ typedef struct gemm_rs_info {
   int32_t ag_direct;      /* AG: own shard read from the input, not copied */
   int64_t copy_items;     /* AG: copy items of a fused run */
   int64_t queue_offset;   /* byte offset of the reduce items' debug stamps in the workspace */
+  int64_t half_region;    /* first region (in tile order) computed in half-width tiles; the
+                             region count if none */
 } gemm_rs_info;
 
 /*
@@ -244,11 +251,16 @@ int gemm_rs_get_info(gemm_rs_t plan, gemm_rs_info* info);
 
 /*
  * Tile order used by the GEMM kernels, as a host-only computation (no CUDA
- * call): the idx-th rank tile (0 <= idx < 8*mt*nt) is rank *rank, tile row
- * *mt (rows [mt*T, (mt+1)*T) with T = 128 * mma_ctas), 256-column tile *nt.
- * Uses d->band_m or the automatic band.
+ * call): the idx-th rank tile (0 <= idx < the plan's tile count) is rank
+ * *rank, tile row *mt (rows [mt*T, (mt+1)*T) with T = 128 * mma_ctas),
+ * 256-column tile *nt, and *half (may be NULL) = -1 for the whole tile, 0 or
+ * 1 for the left or right 128 columns of a half-width tile.  Row-parallel
+ * order: 8 rank tiles per region (ranks 0..7), regions in L2 bands; the last
+ * half_regions regions as 16 half-width tiles each (left halves of ranks
+ * 0..7, then right halves).  Uses d->band_m or the automatic band.
  */
-int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt, int32_t* nt);
+int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt, int32_t* nt,
+                     int32_t* half);
 
 /*
  * Fused run that allocates nothing.  The pages have no counterpart: this is a
@@ -297,7 +309,7 @@ int gemm_rs_destroy(gemm_rs_t plan);
  *     {8, 16} (all-gather: mma_ctas in {2, 1} x copy warps in {1, 2, 4});
  *   d with band_m (the tile-order swizzle band) at 1/2 and 1/4 of the
  *     automatic band;
- *   reduce-scatter: d with tail_waves in {1, 2, 6};
+ *   reduce-scatter: d with tail_waves in {1, 2, 6}, and half_regions in {5, 10};
  * every other field as in d (zeros stand for the defaults).  gemm_rs_tune_candidates
  * writes up to `max` of them to `cands` (may be NULL), sets *count, and
  * *workspace_bytes (may be NULL) to the largest workspace any of them needs.

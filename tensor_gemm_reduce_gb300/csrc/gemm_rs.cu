@@ -88,6 +88,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->op != GEMM_RS_OP_RS && d->op != GEMM_RS_OP_AG) return GEMM_RS_ERR_INVALID_ARG;
   if (d->adaptive != 0 && d->adaptive != 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->tail_waves < 0 || d->tail_waves > 64) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->half_regions < -1 || d->half_regions > 4096) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op == GEMM_RS_OP_AG && d->replicas > 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
@@ -259,7 +260,7 @@ struct gemm_rs_plan_s {
   int device = 0, num_sms = 0;
   int pair = 2, tile_rows = 256;
   int grid = 0, reducer_warps = 0, band = 1, unit_rows = 16, splits = 8, blocks_per_region = 2;
-  long long tail_region = 0;
+  long long tail_region = 0, half_region = 0;
   int mt = 0, nt = 0, num_kb = 0;
   long long tiles = 0, items = 0;
   Layout lay;
@@ -302,31 +303,27 @@ const char* gemm_rs_strerror(int code) {
 }
 
 int gemm_rs_schedule(const gemm_rs_desc* d, int64_t idx, int32_t* rank, int32_t* mt,
-                     int32_t* nt) {
+                     int32_t* nt, int32_t* half) {
   int rc = check_desc(d);
   if (rc) return rc;
   if (!rank || !mt || !nt) return GEMM_RS_ERR_INVALID_ARG;
-  const int tile_rows = kBM * mma_ctas_of(d);
+  const int pair = mma_ctas_of(d);
+  const int tile_rows = kBM * pair;
   const bool ag = d->op == GEMM_RS_OP_AG;
   const int64_t cols = ag ? d->N / kWorld : d->N;
   const int mtc = (int)((d->M + tile_rows - 1) / tile_rows), ntc = (int)((cols + kBN - 1) / kBN);
-  const long long tiles = (long long)kWorld * mtc * ntc;
+  const long long regions = (long long)mtc * ntc;
+  const long long half_region = (!ag && pair == 2) ? half_region_of(regions, d->half_regions) : regions;
+  const long long tiles = tiles_of(regions, half_region);
   if (idx < 0 || idx >= tiles) return GEMM_RS_ERR_INVALID_ARG;
-  if (ag) {  // rank after rank, own shard first, in bands
-    const int band =
-        d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K, tile_rows);
-    const TileCoord t = ag_tile_at(idx, mtc, ntc, (int)(d->M / kWorld), tile_rows, band);
-    *rank = t.rank;
-    *mt = t.mt;
-    *nt = t.nt;
-    return GEMM_RS_OK;
-  }
   const int band =
       d->band_m > 0 ? (d->band_m < mtc ? d->band_m : mtc) : auto_band(d->M, d->K, tile_rows);
-  const TileCoord t = tile_at(idx, mtc, ntc, band);
+  const TileCoord t = ag ? ag_tile_at(idx, mtc, ntc, (int)(d->M / kWorld), tile_rows, band)
+                         : tile_at(idx, mtc, ntc, band, half_region);
   *rank = t.rank;
   *mt = t.mt;
   *nt = t.nt;
+  if (half) *half = t.half;
   return GEMM_RS_OK;
 }
 
@@ -370,7 +367,11 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   h->mt = (int)((d->M + h->tile_rows - 1) / h->tile_rows);
   h->nt = (int)((d->N + kBN - 1) / kBN);
   h->num_kb = (int)((d->K / kWorld + kBK - 1) / kBK);
-  h->tiles = (long long)kWorld * h->mt * h->nt;
+  // the last regions in half-width tiles (CTA-pair tiles of the row-parallel layer)
+  const long long regions = (long long)h->mt * h->nt;
+  h->half_region = (d->op == GEMM_RS_OP_RS && pair == 2) ? half_region_of(regions, d->half_regions)
+                                                        : regions;
+  h->tiles = tiles_of(regions, h->half_region);
   h->grid = grid;
   h->reducer_warps = reducer_warps;
   h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt)
@@ -380,7 +381,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   h->splits = kBM / h->unit_rows;
   h->blocks_per_region = h->tile_rows / kBM;
   const long long blocks = (long long)h->mt * h->nt * h->blocks_per_region;
-  h->tail_region = tail_region_of(h->tiles, h->grid / pair, (long long)h->mt * h->nt,
+  h->tail_region = tail_region_of(kWorld * regions, h->grid / pair, regions,
                                   d->tail_waves > 0 ? d->tail_waves : kDefaultTailWaves);
   h->items = items_of(blocks, h->blocks_per_region, h->tail_region, h->splits);
   h->lay = layout_for(d->M, d->N, blocks, h->items);
@@ -398,6 +399,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
     h->nt = (int)((cols + kBN - 1) / kBN);
     h->num_kb = (int)((d->K + kBK - 1) / kBK);
     h->tiles = (long long)kWorld * h->mt * h->nt;
+    h->half_region = (long long)h->mt * h->nt;  // no half-width tiles
     // bands inside one rank's GEMM: A rows of that rank's gathered buffer
     h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt)
                             : auto_band(d->M, d->K, h->tile_rows);
@@ -454,6 +456,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->mma_ctas = h->pair;
   info->tile_rows = h->tile_rows;
   info->trace_offset = (int64_t)h->lay.trace_off;
+  info->half_region = h->half_region;
   return GEMM_RS_OK;
 }
 
@@ -465,7 +468,7 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
   const bool ag = d->op == GEMM_RS_OP_AG;
   // A candidate is d with some of these fields changed; zeros mean the defaults.
   struct Knobs {
-    int ctas, warps, units, band, tail;
+    int ctas, warps, units, band, tail, half;
   };
   auto resolve = [&](Knobs k) {
     Knobs r;
@@ -479,6 +482,7 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
     const int ab = auto_band(d->M, d->K, tile_rows);
     r.band = k.band > 0 ? (k.band < mtc ? k.band : (mtc > 0 ? mtc : 1)) : ab;
     r.tail = ag ? 0 : (k.tail > 0 ? k.tail : kDefaultTailWaves);
+    r.half = (ag || r.ctas != 2 || k.half < 0) ? 0 : k.half;
     return r;
   };
   Knobs list[GEMM_RS_TUNE_MAX];
@@ -488,30 +492,39 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
     for (int i = 0; i < n; ++i) {
       const Knobs q = resolve(list[i]);
       if (q.ctas == r.ctas && q.warps == r.warps && q.units == r.units && q.band == r.band &&
-          q.tail == r.tail)
+          q.tail == r.tail && q.half == r.half)
         return;  // same plan as an earlier candidate
     }
     if (n < GEMM_RS_TUNE_MAX) list[n++] = k;
   };
   // the requested plan first, then tile shape x communication warps (x item rows)
-  add({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, d->tail_waves});
+  add({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, d->tail_waves, d->half_regions});
   static const int kCtas[2] = {2, 1};
   static const int kWarpsRs[3] = {2, 4, 5}, kWarpsAg[3] = {1, 2, 4};
   static const int kUnits[2] = {8, 16};
   for (int c = 0; c < 2; ++c)
     for (int w = 0; w < 3; ++w)
       for (int u = 0; u < (ag ? 1 : 2); ++u)
-        add({kCtas[c], ag ? kWarpsAg[w] : kWarpsRs[w], ag ? 0 : kUnits[u], d->band_m, d->tail_waves});
+        add({kCtas[c], ag ? kWarpsAg[w] : kWarpsRs[w], ag ? 0 : kUnits[u], d->band_m, d->tail_waves,
+             d->half_regions});
   // tile-order swizzle: narrower L2 bands than the automatic one (FLUX page,
   // TL;DR: tile coordinate swizzling), for the requested tile shape and warps
   {
-    const Knobs r = resolve({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, d->tail_waves});
+    const Knobs r = resolve({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, d->tail_waves,
+                             d->half_regions});
     const int ab = auto_band(d->M, d->K, kBM * r.ctas);
     for (int div = 2; div <= 4; div *= 2)
-      if (ab / div >= 1) add({d->mma_ctas, d->reducer_warps, d->unit_rows, ab / div, d->tail_waves});
+      if (ab / div >= 1)
+        add({d->mma_ctas, d->reducer_warps, d->unit_rows, ab / div, d->tail_waves, d->half_regions});
     // how many final waves of regions are reduced in 4-row items
     if (!ag)
-      for (int t : {1, 2, 6}) add({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, t});
+      for (int t : {1, 2, 6})
+        add({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, t, d->half_regions});
+    // final regions computed in half-width tiles (about one and two waves of
+    // half tiles on 76 CTA pairs)
+    if (!ag)
+      for (int hr : {5, 10})
+        add({d->mma_ctas, d->reducer_warps, d->unit_rows, d->band_m, d->tail_waves, hr});
   }
   size_t ws_max = 0;
   for (int i = 0; i < n; ++i) {
@@ -521,6 +534,7 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
     e.unit_rows = list[i].units;
     e.band_m = list[i].band;
     e.tail_waves = list[i].tail;
+    e.half_regions = list[i].half;
     if (cands && i < max) cands[i] = e;
     // the workspace size depends only on the shape, the tile shape and the item count
     const int tile_rows = kBM * mma_ctas_of(&e);
@@ -707,7 +721,9 @@ static int run_chunked(gemm_rs_t h, const void* A, void* out, void* ws, cudaStre
       return GEMM_RS_ERR_CUDA;
     p.M = (int)rows;
     p.mt_count = (int)((rows + h->tile_rows - 1) / h->tile_rows);
-    p.num_tiles = (long long)kWorld * p.mt_count * h->nt;
+    const long long chunk_regions = (long long)p.mt_count * h->nt;
+    p.half_region = (int)(h->pair == 2 ? half_region_of(chunk_regions, d.half_regions) : chunk_regions);
+    p.num_tiles = tiles_of(chunk_regions, p.half_region);
     p.band = d.band_m > 0 ? (d.band_m < p.mt_count ? d.band_m : p.mt_count)
                           : auto_band(rows, d.K, h->tile_rows);
     if (p.band < 1) p.band = 1;
@@ -811,6 +827,7 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
   p.blocks_per_region = h->blocks_per_region;
   p.tile_rows = h->tile_rows;
   p.num_tiles = h->tiles;
+  p.half_region = (int)h->half_region;
   p.debug_flags = d.debug_flags;
   p.timeout_ns = d.timeout_ns;
   p.trace = (d.debug_flags & GEMM_RS_DEBUG_TRACE)
@@ -918,6 +935,7 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
     p.splits = h->splits;
     p.blocks_per_region = h->blocks_per_region;
     p.tail_region = (int)h->tail_region;
+    p.half_region = (int)h->half_region;
     p.tile_rows = h->tile_rows;
     p.num_tiles = h->tiles;
     p.num_items = h->items;
@@ -946,8 +964,6 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
                                 !(d.debug_flags & GEMM_RS_DEBUG_NO_STAGING_L2);
       h->epoch += 1;
       h->params.epoch = h->epoch;
-      // every epilogue warp of every rank adds 1 per block and run
-      h->params.flag_target = (uint32_t)(kWorld * kEpiWarps) * h->epoch;
       rc = launch_gemm(h, true, st);
       break;
     case GEMM_RS_UNFUSED:
@@ -1175,12 +1191,12 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.splits = kBM / kDefaultUnitRows;
     p.blocks_per_region = tile_rows / kBM;
     p.tile_rows = tile_rows;
-    p.num_tiles = (long long)kWorld * mt * nt;
+    p.half_region = (int)half_region_of(mt * nt, 0);
+    p.num_tiles = tiles_of(mt * nt, p.half_region);
     const long long tail =
-        tail_region_of(p.num_tiles, nd->grid / kDefaultMmaCtas, mt * nt, kDefaultTailWaves);
+        tail_region_of(kWorld * mt * nt, nd->grid / kDefaultMmaCtas, mt * nt, kDefaultTailWaves);
     p.tail_region = (int)tail;
     p.num_items = items_of(blocks, p.blocks_per_region, tail, p.splits);
-    p.flag_target = (uint32_t)(kWorld * kEpiWarps);  // counts were just cleared: one run's adds
     p.timeout_ns = kDefaultTimeoutNs;
     rc = launch_gemm_kernel(kDefaultMmaCtas, kKindRS, nd->grid,
                             32 * cta_warps(kDefaultReducerWarps), p, st);

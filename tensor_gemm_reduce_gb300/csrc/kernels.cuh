@@ -178,6 +178,10 @@ struct GemmParams {
   // many warps.  Item positions: tail_region * blocks_per_region * splits
   // unit_rows-row items, then 32 4-row items per block of the tail regions.
   int tail_region;
+  // Regions from order position half_region on are computed in half-width
+  // tiles (tile_at); each of their blocks then receives 64 release adds per
+  // run instead of 32.  The number of regions if none.
+  int half_region;
   long long num_tiles;
   long long num_items;    // reduce items of a run
   // Debug stamps of each item (GEMM_RS_DEBUG_TRACE only), kQueueStride words
@@ -262,7 +266,14 @@ struct Item {
   int block;  // 128-row block: (physical region) * blocks_per_region + CTA of the pair
   int part;   // which rows of the block
   int rows;   // unit_rows, or 4 in the tail regions
+  int g;      // the region's position in the order
 };
+
+// Release adds a block receives per run: 8 ranks x 4 epilogue warps, twice
+// that in the regions computed in half-width tiles.
+__device__ __forceinline__ uint32_t adds_per_run(const GemmParams& p, long long g) {
+  return (uint32_t)(kWorld * kEpiWarps) * (g >= p.half_region ? 2u : 1u);
+}
 
 // The item at order position pos (0 <= pos < num_items): regions in the order
 // the tiles complete them (tile_at's region order), each region's blocks in
@@ -287,6 +298,7 @@ __device__ __forceinline__ Item item_at(const GemmParams& p, long long pos) {
     it.rows = 4;
   }
   const Region reg = region_at(g, p.mt_count, p.nt_count, p.band);
+  it.g = (int)g;
   it.block = (reg.mt * p.nt_count + reg.nt) * p.blocks_per_region + (int)(r / per_block);
   it.part = (int)(r % per_block);
   return it;
@@ -294,13 +306,15 @@ __device__ __forceinline__ Item item_at(const GemmParams& p, long long pos) {
 
 // First order position of a block's items, and how many it has (the inverse
 // of item_at; used only to stamp the debug timeline).
-__device__ __forceinline__ long long first_item_of(const GemmParams& p, int block, int* count) {
+__device__ __forceinline__ long long first_item_of(const GemmParams& p, int block, int* count,
+                                                   long long* g_out) {
   const int phys = block / p.blocks_per_region;
   const int rb = block - phys * p.blocks_per_region;
   const int mt = phys / p.nt_count, nt = phys - (phys / p.nt_count) * p.nt_count;
   const int b = mt / p.band, mt0 = b * p.band;
   const int h = (p.mt_count - mt0) < p.band ? (p.mt_count - mt0) : p.band;
   const long long g = (long long)b * p.band * p.nt_count + (long long)nt * h + (mt - mt0);
+  *g_out = g;
   const long long per_region = (long long)p.blocks_per_region * p.splits;
   if (g < p.tail_region) {
     *count = p.splits;
@@ -326,12 +340,13 @@ __device__ __forceinline__ int item_pop(const GemmParams& p, int lane, Item* it,
   *it = item_at(p, pos);
   *pos_out = pos;
   const uint32_t* cnt = p.flags + (size_t)it->block * kFlagStride;
+  const uint32_t target = adds_per_run(p, it->g) * p.epoch;  // this run's adds, counted since clearing
   uint64_t t0 = 0;
   if (lane == 0) t0 = globaltimer_ns();
   uint32_t sleep_ns = 32;
   while (true) {
     int ready = 0;
-    if (lane == 0) ready = (int)(ld_acquire_gpu(cnt) - p.flag_target) >= 0;
+    if (lane == 0) ready = (int)(ld_acquire_gpu(cnt) - target) >= 0;
     if (__shfl_sync(0xffffffffu, ready, 0)) {
       __syncwarp();
       return 1;
@@ -509,9 +524,10 @@ __device__ __forceinline__ void publish_rows(const GemmParams& p, int block, boo
     red_release_gpu_add(cnt, 1u);
     return;
   }
-  if (atom_add_release_gpu(cnt, 1u) == p.flag_target - 1u) {
-    int n = 0;
-    const long long first = first_item_of(p, block, &n);
+  int n = 0;
+  long long g = 0;
+  const long long first = first_item_of(p, block, &n, &g);
+  if (atom_add_release_gpu(cnt, 1u) == adds_per_run(p, g) * p.epoch - 1u) {
     const uint64_t now = globaltimer_ns();
     for (int i = 0; i < n; ++i) st_relaxed_gpu_u64(p.queue + (size_t)(first + i) * kQueueStride + 1, now);
   }
@@ -694,7 +710,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
   auto coord = [&](int idx) {
     return (kAG || p.ag_order)
                ? ag_tile_at(idx, p.mt_count, p.nt_count, p.shard_rows, C::kTileRows, p.band)
-               : tile_at(idx, p.mt_count, p.nt_count, p.band);
+               : tile_at(idx, p.mt_count, p.nt_count, p.band, p.half_region);
   };
 
   if (threadIdx.x == 0) {
@@ -765,7 +781,13 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
         if (idx < 0) break;
         const TileCoord tc = coord(idx);
         const int m0 = tc.mt * C::kTileRows + (int)cta_rank * kBM;
-        const int n0 = tc.nt * kBN + (int)half * C::kBCols;
+        // a half-width tile is the left or right 128 of the 256 columns: each CTA
+        // loads half as many columns of W
+        const bool half_tile = tc.half >= 0;
+        const int cta_cols = (half_tile ? kBN / 2 : kBN) / kPair;
+        const int n0 = tc.nt * kBN + (half_tile ? tc.half * (kBN / 2) : 0) + (int)half * cta_cols;
+        const int nboxes = cta_cols / 64;
+        const uint32_t stage_bytes = (uint32_t)(C::kAStage + nboxes * C::kBBoxBytes);
         const CUtensorMap* amap = &p.tmap_a;
         int arow = m0;
         if constexpr (kAG) {
@@ -798,18 +820,16 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
           const uint32_t sa = sbase + C::kSmemA + stage * C::kAStage;
           const uint32_t sb = sbase + C::kSmemB + stage * C::kBStage;
           if constexpr (kCtas == 1) {
-            mbar_arrive_expect_tx(fb, C::kStage);
+            mbar_arrive_expect_tx(fb, stage_bytes);
             tma_load_3d(sa, amap, fb, kb * kBK, arow, tc.rank);
-#pragma unroll
-            for (int j = 0; j < C::kBBoxes; ++j)
+            for (int j = 0; j < nboxes; ++j)
               tma_load_3d(sb + j * C::kBBoxBytes, &p.tmap_b, fb, n0 + 64 * j, kb * kBK, tc.rank);
           } else {
             // both CTAs' bytes are counted on the leader's barrier
-            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kStage);
+            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * stage_bytes);
             const uint32_t fb_leader = mapa_shared(fb, 0);
             tma_load_3d_pair(sa, amap, fb_leader, kb * kBK, arow, tc.rank);
-#pragma unroll
-            for (int j = 0; j < C::kBBoxes; ++j)
+            for (int j = 0; j < nboxes; ++j)
               tma_load_3d_pair(sb + j * C::kBBoxBytes, &p.tmap_b, fb_leader, n0 + 64 * j,
                                kb * kBK, tc.rank);
           }
@@ -833,7 +853,8 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
   } else if (warp == 1) {
     if (lane == 0 && mma_leader) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM * kPair, kBN, /*b_mn_major=*/1);
+      constexpr uint32_t idesc_full = idesc_bf16_f32(kBM * kPair, kBN, /*b_mn_major=*/1);
+      constexpr uint32_t idesc_half = idesc_bf16_f32(kBM * kPair, kBN / 2, /*b_mn_major=*/1);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -856,6 +877,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        const uint32_t idesc = coord(idx).half >= 0 ? idesc_half : idesc_full;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!bar_wait(bar_full + 8 * stage, phase, limit, cta_abort)) {
             if (!*cta_abort) {
@@ -938,8 +960,10 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
       const TileCoord tc = coord(idx);
       tc_fence_after();
       const int row0 = tc.mt * C::kTileRows + (int)cta_rank * kBM + q * 32;  // the warp's first row
+      const int nchunks = tc.half >= 0 ? kBN / 128 : kBN / 64;  // 64-column chunks of the tile
+      const int col0 = tc.nt * kBN + (tc.half >= 0 ? tc.half * (kBN / 2) : 0);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 64; ++c) {
+      for (int c = 0; c < nchunks; ++c) {
         uint32_t v0[32], v1[32];
         const uint32_t taddr =
             tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + c * 64);
@@ -947,7 +971,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
         tmem_ld_32x32b_x32(taddr + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
-        if (c == kBN / 64 - 1) {
+        if (c == nchunks - 1) {
           // accumulator fully read: hand it back to the (leader's) MMA warp
           tc_fence_before();
           __syncwarp();
@@ -958,7 +982,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
               mbar_arrive_remote(mapa_shared(bar_acc_empty + 8 * acc, mma_leader_rank));
           }
         }
-        const int col = tc.nt * kBN + c * 64;
+        const int col = col0 + c * 64;
         if (row0 < p.M && col < p.N) {  // warp-uniform; the store clips ragged edges
           const uint32_t buf = lane_row + (uint32_t)nbuf * kEpiBufBytes;
           if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it

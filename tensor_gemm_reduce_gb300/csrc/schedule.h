@@ -52,16 +52,50 @@ GRS_HD Region region_at(int64_t p, int mt_count, int nt_count, int band) {
 
 struct TileCoord {
   int rank, mt, nt;
+  int half;  // -1: the whole tile; 0 / 1: its left / right half (columns [0, 128) / [128, 256))
 };
 
-// Rank tile at order position idx (0 <= idx < 8*mt_count*nt_count).
-GRS_HD TileCoord tile_at(int64_t idx, int mt_count, int nt_count, int band) {
-  const Region g = region_at(idx / kWorld, mt_count, nt_count, band);
+// Optionally the last regions of the order are computed in half-width tiles
+// (2 per rank tile, so 16 per region): a final wave of tiles half as long
+// halves the spread of the CTAs' finishing times and the last tile's
+// epilogue, after which only the last regions' reduction is left.
+// Rank tiles before region half_region: 8 per region, ranks 0..7; from
+// half_region on: 16 per region, the left halves of ranks 0..7, then the
+// right halves.  Tile count of an order with `regions` regions:
+GRS_HD int64_t tiles_of(int64_t regions, int64_t half_region) {
+  return (int64_t)kWorld * half_region + 2 * (int64_t)kWorld * (regions - half_region);
+}
+
+// Rank tile at order position idx (0 <= idx < tiles_of(mt_count*nt_count, half_region)).
+GRS_HD TileCoord tile_at(int64_t idx, int mt_count, int nt_count, int band, int64_t half_region) {
+  const int64_t full = (int64_t)kWorld * half_region;
+  int64_t g;
   TileCoord t;
-  t.rank = (int)(idx % kWorld);
-  t.mt = g.mt;
-  t.nt = g.nt;
+  if (idx < full) {
+    g = idx / kWorld;
+    t.rank = (int)(idx % kWorld);
+    t.half = -1;
+  } else {
+    const int64_t q = idx - full;
+    g = half_region + q / (2 * kWorld);
+    const int r16 = (int)(q % (2 * kWorld));
+    t.half = r16 / kWorld;
+    t.rank = r16 % kWorld;
+  }
+  const Region r = region_at(g, mt_count, nt_count, band);
+  t.mt = r.mt;
+  t.nt = r.nt;
   return t;
+}
+
+// First region in half-width tiles for a request of `half_regions` regions
+// (0 or negative: none), clamped to the regions there are.  None is the
+// default: measured with 1 to 9 half-width regions, the shorter final wave
+// did not pay for the half-width tiles' lower throughput (they load 24 KiB
+// per 256-cycle k-step instead of 32 KiB per 512) on o_proj-sized shapes.
+GRS_HD int64_t half_region_of(int64_t regions, int half_regions) {
+  const int64_t want = half_regions < 0 ? 0 : half_regions;
+  return want >= regions ? 0 : regions - want;
 }
 
 // AllGather + GEMM (mKernel page, section 4: the local shard first, then
@@ -75,6 +109,7 @@ GRS_HD TileCoord ag_tile_at(int64_t idx, int mt_count, int nt_count, int shard_r
                             int tile_rows, int band) {
   const int64_t per_rank = (int64_t)mt_count * nt_count;
   TileCoord t;
+  t.half = -1;
   t.rank = (int)(idx / per_rank);
   const Region g = region_at(idx - t.rank * per_rank, mt_count, nt_count, band);
   const int start = (int)(((int64_t)t.rank * shard_rows) / tile_rows);

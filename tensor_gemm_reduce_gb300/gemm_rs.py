@@ -65,6 +65,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("op", ctypes.c_int32),
         ("adaptive", ctypes.c_int32),
         ("tail_waves", ctypes.c_int32),
+        ("half_regions", ctypes.c_int32),
     ]
 
 
@@ -93,6 +94,7 @@ class gemm_rs_info(ctypes.Structure):
         ("ag_direct", ctypes.c_int32),
         ("copy_items", ctypes.c_int64),
         ("queue_offset", ctypes.c_int64),
+        ("half_region", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -120,7 +122,7 @@ _SIGS = {
     "gemm_rs_get_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(gemm_rs_info)]),
     "gemm_rs_schedule": (ctypes.c_int, [ctypes.POINTER(gemm_rs_desc), ctypes.c_int64,
                                         ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
-                                        ctypes.POINTER(ctypes.c_int32)]),
+                                        ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "gemm_rs_fused_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_void_p, ctypes.c_void_p]),
@@ -177,9 +179,10 @@ def strerror(code: int) -> str:
 
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
-          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, adaptive=0, tail_waves=0, world=WORLD):
+          mma_ctas=0, chunks=0, replicas=0, op=OP_RS, adaptive=0, tail_waves=0, half_regions=0,
+          world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas, chunks, replicas, op, adaptive, tail_waves)
+                        debug_flags, mma_ctas, chunks, replicas, op, adaptive, tail_waves, half_regions)
 
 
 # ----------------------------------------------------------------------------
@@ -221,12 +224,14 @@ def gemm_rs_get_info(plan) -> gemm_rs_info:
 
 
 def gemm_rs_schedule(desc: gemm_rs_desc, idx: int):
-    r, m, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    """(rank, tile row, 256-column tile, half) of the idx-th rank tile; half is
+    -1 for a whole tile, 0 / 1 for the left / right half of a half-width one."""
+    r, m, n, h = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     rc = load_library().gemm_rs_schedule(ctypes.byref(desc), idx, ctypes.byref(r), ctypes.byref(m),
-                                         ctypes.byref(n))
+                                         ctypes.byref(n), ctypes.byref(h))
     if rc != GEMM_RS_OK:
         raise GemmRSError(rc, "gemm_rs_schedule")
-    return r.value, m.value, n.value
+    return r.value, m.value, n.value, h.value
 
 
 def gemm_rs_fused_noalloc(A_ptr: int, W_ptr: int, out_ptr: int, M: int, N: int, K: int,
@@ -258,13 +263,13 @@ class Plan:
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
                  mma_ctas: int = 0, chunks: int = 0, replicas: int = 0, op: int = OP_RS,
-                 adaptive: int = 0, tail_waves: int = 0):
+                 adaptive: int = 0, tail_waves: int = 0, half_regions: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.replicas = max(1, int(replicas))
         self.op = int(op)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
                           timeout_ns, debug_flags, mma_ctas, chunks, replicas, op, adaptive,
-                          tail_waves)
+                          tail_waves, half_regions)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property
@@ -419,7 +424,7 @@ def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Pl
 
 TUNE_MAX = 32
 _DESC_KW = ("reducer_warps", "grid", "band_m", "unit_rows", "timeout_ns", "debug_flags",
-            "mma_ctas", "chunks", "replicas", "op", "adaptive", "tail_waves")
+            "mma_ctas", "chunks", "replicas", "op", "adaptive", "tail_waves", "half_regions")
 
 
 def tune_candidates(desc: gemm_rs_desc):

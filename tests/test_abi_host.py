@@ -61,6 +61,7 @@ def _create(**kw):
     (dict(chunks=65), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(replicas=2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(tail_waves=65), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(half_regions=-2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(tail_waves=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=G.OP_AG, replicas=8), G.GEMM_RS_ERR_INVALID_ARG),
@@ -94,34 +95,51 @@ def test_strerror(lib):
 
 
 @pytest.mark.parametrize("ctas", [1, 2])
+@pytest.mark.parametrize("half", [0, -1, 3, 4000])
 @pytest.mark.parametrize("M,N,K,band", [(128, 512, 1024, 0), (392, 776, 1600, 0),
                                         (2048, 8192, 8192, 0), (8192, 8192, 28672, 0),
                                         (1000, 6144, 6144, 3), (520, 1000, 1024, 1)])
-def test_schedule_covers_every_tile_once(lib, M, N, K, band, ctas):
-    d = G._desc(M, N, K, band_m=band, mma_ctas=ctas)
+def test_schedule_covers_every_tile_once(lib, M, N, K, band, ctas, half):
+    """Every rank tile exactly once: whole tiles (8 per region, ranks in
+    order) first, then the last regions as half-width tiles (16 per region:
+    the left halves of ranks 0..7, then the right halves), which together
+    cover the same columns."""
+    d = G._desc(M, N, K, band_m=band, mma_ctas=ctas, half_regions=half)
     rows = 128 * ctas
     mt, nt = (M + rows - 1) // rows, (N + 255) // 256
-    seen = set()
-    order = []
-    for i in range(8 * mt * nt):
-        r, m, n = G.gemm_rs_schedule(d, i)
-        assert 0 <= r < 8 and 0 <= m < mt and 0 <= n < nt
-        seen.add((r, m, n))
-        order.append((r, m, n))
-    assert len(seen) == 8 * mt * nt
-    # the 8 rank tiles of a region are consecutive, ranks in order
-    for g in range(mt * nt):
+    regions = mt * nt
+    want = max(half, 0)  # 0 (default) and -1: none
+    n_half = min(want, regions) if ctas == 2 else 0     # regions in half-width tiles
+    first_half = regions - n_half
+    tiles = 8 * first_half + 16 * n_half
+    order = [G.gemm_rs_schedule(d, i) for i in range(tiles)]
+    assert len(set(order)) == tiles
+    for r, m, n, h in order:
+        assert 0 <= r < 8 and 0 <= m < mt and 0 <= n < nt and h in (-1, 0, 1)
+    covered = {(r, m, n, c) for r, m, n, h in order for c in ((0, 1) if h < 0 else (h,))}
+    assert len(covered) == 8 * regions * 2  # every rank's both column halves of every region once
+    for g in range(first_half):
         blk = order[8 * g: 8 * g + 8]
-        assert [b[0] for b in blk] == list(range(8))
+        assert [b[0] for b in blk] == list(range(8)) and {b[3] for b in blk} == {-1}
         assert len({(b[1], b[2]) for b in blk}) == 1
+    for k in range(n_half):
+        blk = order[8 * first_half + 16 * k: 8 * first_half + 16 * (k + 1)]
+        assert [b[0] for b in blk] == list(range(8)) * 2
+        assert [b[3] for b in blk] == [0] * 8 + [1] * 8
+        assert len({(b[1], b[2]) for b in blk}) == 1
+    # half-width tiles take the regions that come last in the whole-tile order
+    d_none = G._desc(M, N, K, band_m=band, mma_ctas=ctas, half_regions=-1)
+    whole = [G.gemm_rs_schedule(d_none, 8 * g)[1:3] for g in range(regions)]
+    assert [order[8 * g][1:3] for g in range(first_half)] == whole[:first_half]
+    assert [order[8 * first_half + 16 * k][1:3] for k in range(n_half)] == whole[first_half:]
     with pytest.raises(G.GemmRSError):
-        G.gemm_rs_schedule(d, 8 * mt * nt)
+        G.gemm_rs_schedule(d, tiles)
 
 
 def test_schedule_band_walks_columns_inside_band(lib):
     # band of 4 tile rows: positions 0..3 are column 0, rows 0..3
     d = G._desc(1024, 1024, 1024, band_m=4, mma_ctas=1)
-    regions = [G.gemm_rs_schedule(d, 8 * g)[1:] for g in range(8 * 4)]
+    regions = [G.gemm_rs_schedule(d, 8 * g)[1:3] for g in range(8 * 4)]
     assert regions[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
     assert regions[16] == (4, 0)
 
@@ -135,7 +153,7 @@ def test_auto_band_keeps_a_rows_within_budget(lib, ctas):
         mt = (M + rows - 1) // rows
         band = None
         for g in range(mt * 4):
-            _, m, n = G.gemm_rs_schedule(d, 8 * g)
+            _, m, n, _ = G.gemm_rs_schedule(d, 8 * g)
             if n == 1:
                 band = g
                 break
@@ -154,7 +172,7 @@ def test_ag_schedule_walks_from_own_shard(lib, M, N, K, ctas):
     mt, nt = (M + rows - 1) // rows, (N // 8 + 255) // 256
     seen = []
     for i in range(8 * mt * nt):
-        seen.append(tuple(G.gemm_rs_schedule(d, i)))
+        seen.append(tuple(G.gemm_rs_schedule(d, i)[:3]))
     assert len(set(seen)) == 8 * mt * nt
     per_rank = mt * nt
     for r in range(8):
@@ -172,17 +190,20 @@ def test_tune_candidates_and_their_workspace(lib, op):
     d = G._desc(1024, 2048, 4096, op=op, timeout_ns=7)
     cands, ws = G.tune_candidates(d)
     # auto band at M=1024, K=4096, 256-row tiles: 32 MiB / (256*4096*2) = 16 -> 4 tile rows
-    assert len(cands) == (1 + 11 + 2 + 3 if op == 0 else 1 + 5 + 2)
+    assert len(cands) == (1 + 11 + 2 + 3 + 2 if op == 0 else 1 + 5 + 2)
     c0 = cands[0]
     assert (c0.mma_ctas, c0.reducer_warps, c0.unit_rows, c0.band_m, c0.tail_waves) == (0, 0, 0, 0, 0)
     def resolved(c):
-        return (c.mma_ctas or 2, c.reducer_warps or (4 if op == 0 else 2),  # K = 4096 < 16384
-                (c.unit_rows or 8) if op == 0 else 0, c.band_m or (4 if (c.mma_ctas or 2) == 2 else 8),
-                (c.tail_waves or 3) if op == 0 else 0)
+        ctas = c.mma_ctas or 2
+        return (ctas, c.reducer_warps or (4 if op == 0 else 2),  # K = 4096 < 16384
+                (c.unit_rows or 8) if op == 0 else 0, c.band_m or (4 if ctas == 2 else 8),
+                (c.tail_waves or 3) if op == 0 else 0,
+                max(c.half_regions, 0) if (op == 0 and ctas == 2) else 0)
     assert len({resolved(c) for c in cands}) == len(cands)
     assert {c.band_m for c in cands} >= {0, 1, 2}
     if op == 0:
         assert {c.tail_waves for c in cands} >= {0, 1, 2, 6}
+        assert {c.half_regions for c in cands} == {0, 5, 10}
     assert all(c.M == 1024 and c.N == 2048 and c.K == 4096 and c.op == op and c.timeout_ns == 7
                for c in cands)
     staging = 8 * 1024 * (2048 if op == 0 else 4096) * 2

@@ -70,7 +70,9 @@ def test_ragged_and_small_shapes(M, N, K):
                                 dict(grid=8, reducer_warps=2),
                                 dict(adaptive=1), dict(adaptive=1, reducer_warps=5, unit_rows=8),
                                 dict(adaptive=1, mma_ctas=1, grid=5),
-                                dict(unit_rows=4, tail_waves=1), dict(unit_rows=16, tail_waves=64)])
+                                dict(unit_rows=4, tail_waves=1), dict(unit_rows=16, tail_waves=64),
+                                dict(half_regions=-1), dict(half_regions=1), dict(half_regions=4000),
+                                dict(half_regions=4000, unit_rows=16, tail_waves=1)])
 def test_plan_variants(kw):
     A, W = workloads.make_shape_inputs(520, 1000, 1024, seed=9)
     _full_check(A, W, **kw)
@@ -447,3 +449,22 @@ def test_fused_on_workspace_off_a_line_boundary(offset):
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     exp, _ = oracle.gemm_rs(A, W)
     assert_parity(to_host_values(out), exp, None)
+
+
+@pytest.mark.parametrize("M,N,K", [(392, 776, 1600), (1024, 1280, 2048), (264, 1536, 2048)])
+def test_half_width_tiles_match_whole_tiles(M, N, K):
+    """A region computed as two half-width tiles (256 x 128 MMAs) gives the same
+    per-rank partials and the same output bits as one whole tile: the MMA's
+    per-element K accumulation does not depend on the tile's width."""
+    A, W = workloads.make_shape_inputs(M, N, K, seed=M + 7 * N + K)
+    whole = Case(A, W, half_regions=-1)
+    halves = Case(A, W, half_regions=4000)
+    assert whole.plan.info.half_region == whole.plan.info.mt * whole.plan.info.nt
+    assert halves.plan.info.half_region == 0
+    for mode in (G.UNFUSED, G.FUSED):
+        a = whole.run(mode, poison=True)
+        b = halves.run(mode, poison=True)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), mode
+    whole.run(G.GEMM_ONLY, poison=True)
+    halves.run(G.GEMM_ONLY, poison=True)
+    assert torch.equal(whole.staging().view(torch.int16), halves.staging().view(torch.int16))
