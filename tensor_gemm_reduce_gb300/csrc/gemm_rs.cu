@@ -102,7 +102,8 @@ int check_desc(const gemm_rs_desc* d) {
   }
   const int64_t cols = d->op == GEMM_RS_OP_AG ? d->N / kWorld : d->N;
   const int64_t mt = (d->M + kBM - 1) / kBM, nt = (cols + kBN - 1) / kBN;
-  if (mt * nt * kWorld >= (1ll << 31)) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
+  // tile order positions (half-width tiles count twice) stay below 2^31
+  if (mt * nt * kWorld >= (1ll << 30)) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   return GEMM_RS_OK;
 }
 
@@ -132,6 +133,28 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// W [8][rows][cols] as the 4-D map of GemmParams::tmap_w4: one box holds a
+// CTA's columns of a 64-row stage (pair: 128 columns, one CTA: 256) as
+// consecutive 8 KiB blocks of 64 columns, the layout the 3-D boxes gave.
+// Leaves p->w4 = 0 (the kernel then copies 64 columns at a time) when the
+// rows are not whole 64-column blocks.
+bool make_map_w4(GemmParams* p, const void* w, uint64_t cols, uint64_t rows, int pair) {
+  p->w4 = 0;
+  if (cols % 64) return true;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, rows, cols / 64, (cuuint64_t)kWorld};
+  cuuint64_t strides[3] = {cols * 2, 128, cols * 2 * rows};
+  cuuint32_t box[4] = {64, (cuuint32_t)kBK, (cuuint32_t)(kBN / pair / 64), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(&p->tmap_w4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  p->w4 = 1;
+  return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -427,7 +450,7 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
   info->num_sms = h->num_sms;
   info->grid = h->grid;
   info->threads_fused = 32 * cta_warps(h->reducer_warps);
-  info->threads_gemm = 32 * kGemmWarps;
+  info->threads_gemm = 32 * cta_warps(0);
   info->smem_bytes = gemm_smem_max(h->pair);
   info->band_m = h->band;
   info->unit_rows = h->unit_rows;
@@ -662,7 +685,7 @@ int gemm_rs_destroy(gemm_rs_t h) {
 
 static int launch_gemm(gemm_rs_t h, bool fused, cudaStream_t st) {
   return launch_gemm_kernel(h->pair, fused ? kKindRS : kKindGemm, h->grid,
-                            32 * (fused ? cta_warps(h->reducer_warps) : kGemmWarps), h->params, st);
+                            32 * cta_warps(fused ? h->reducer_warps : 0), h->params, st);
 }
 
 // Reduce kernel over output rows [row0, row0 + rows).
@@ -729,7 +752,7 @@ static int run_chunked(gemm_rs_t h, const void* A, void* out, void* ws, cudaStre
     if (p.band < 1) p.band = 1;
     p.staging_in_l2 = 0;
     p.trace = nullptr;
-    int rc = launch_gemm_kernel(h->pair, kKindGemm, h->grid, 32 * kGemmWarps, p, st);
+    int rc = launch_gemm_kernel(h->pair, kKindGemm, h->grid, 32 * cta_warps(0), p, st);
     if (rc != GEMM_RS_OK) return rc;
     if (cudaEventRecord(h->ev_chunk[c], st) != cudaSuccess ||
         cudaStreamWaitEvent(h->side, h->ev_chunk[c], 0) != cudaSuccess)
@@ -804,7 +827,8 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
   bool ok = fused ? make_map(&p.tmap_a, A, K, shard, kWorld, K * 2, K * 2 * shard, kBK, kBM) &&
                         make_map(&p.tmap_g, wsb, K, M, kWorld, K * 2, K * 2 * M, kBK, kBM)
                   : make_map(&p.tmap_a, wsb, K, M, kWorld, K * 2, K * 2 * M, kBK, kBM);
-  ok = ok && make_map(&p.tmap_b, W, cols, K, kWorld, cols * 2, cols * 2 * K, 64, kBK);
+  ok = ok && make_map(&p.tmap_b, W, cols, K, kWorld, cols * 2, cols * 2 * K, 64, kBK) &&
+       make_map_w4(&p, W, cols, K, h->pair);
   // epilogue stores into the output [8][M][N/8]: 32 x 64 boxes
   ok = ok && make_map(&p.tmap_s, out, cols, M, kWorld, cols * 2, cols * 2 * M, 64, 32);
   if (!ok) return GEMM_RS_ERR_CUDA;
@@ -858,7 +882,7 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
     const int rc = launch_gather(h, A, wsb, st);
     if (rc != GEMM_RS_OK) return rc;
   }
-  return launch_gemm_kernel(h->pair, kKindGemm, h->grid, 32 * kGemmWarps, p, st);
+  return launch_gemm_kernel(h->pair, kKindGemm, h->grid, 32 * cta_warps(0), p, st);
 }
 
 int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, void* ws,
@@ -910,7 +934,8 @@ int gemm_rs_run(gemm_rs_t h, int mode, const void* A, const void* W, void* out, 
       if (!make_map(&p.tmap_a, a, Kr, (uint64_t)d.M, kWorld, Kr * 2, Kr * 2 * (uint64_t)d.M, kBK,
                     kBM) ||
           !make_map(&p.tmap_b, w, (uint64_t)d.N, Kr, kWorld, (uint64_t)d.N * 2,
-                    (uint64_t)d.N * 2 * Kr, 64, kBK))
+                    (uint64_t)d.N * 2 * Kr, 64, kBK) ||
+          !make_map_w4(&p, w, (uint64_t)d.N, Kr, h->pair))
         return GEMM_RS_ERR_CUDA;
     }
     // epilogue stores into the staging: 32 x 64 boxes
@@ -1164,7 +1189,8 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     const uint64_t Kr = (uint64_t)(K / kWorld);
     if (!make_map(&p.tmap_a, A, Kr, (uint64_t)M, kWorld, Kr * 2, Kr * 2 * (uint64_t)M, kBK, kBM) ||
         !make_map(&p.tmap_b, W, (uint64_t)N, Kr, kWorld, (uint64_t)N * 2, (uint64_t)N * 2 * Kr, 64,
-                  kBK))
+                  kBK) ||
+        !make_map_w4(&p, W, (uint64_t)N, Kr, kDefaultMmaCtas))
       return GEMM_RS_ERR_CUDA;
     if (!make_map(&p.tmap_s, scratch, (uint64_t)N, (uint64_t)M, kWorld, (uint64_t)N * 2,
                   (uint64_t)N * 2 * (uint64_t)M, 64, 32))

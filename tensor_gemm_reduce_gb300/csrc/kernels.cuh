@@ -58,15 +58,22 @@ constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators of 256 columns
 constexpr int kGemmWarps = 2 + kEpiWarps;
 constexpr int kMaxReducerWarps = 5;
 
-// Communication warps (reducers or copy warps) follow the GEMM warps, except
-// that warp 9 is left idle once there are 4 or more of them: warp w runs on
-// the SM sub-partition w % 4, and a reducer beside the MMA warp (warp 1) slows
-// the MMA stream it shares issue slots with (no-load fused runs: 167 cycles per
-// 256x256x16 MMA with a reducer on that sub-partition, 153 without).
-__host__ __device__ constexpr int cta_warps(int comm_warps) {
-  return kGemmWarps + comm_warps + (comm_warps >= 4 ? 1 : 0);
+// Warp roles: 0 loads A (and claims the tiles in the cluster's first CTA),
+// 1 issues the MMAs, 2-5 run the epilogue; then one warp loads W and the
+// communication warps (reducers or copy warps) follow.  The operand loads are
+// split over two threads because one thread issuing both operands' copies
+// could not keep up with the tensor pipe: a 64-wide K step is 512 tensor
+// cycles, and the single loader spent ~365 cycles of it blocked in its TMA
+// issues plus its waits and bookkeeping (GEMM alone, o_proj: 713 cycles per
+// K step with one loader, 625 with two).  Warp w runs on the SM
+// sub-partition w % 4; a reducer beside the MMA warp (warp 1) slows the MMA
+// stream it shares issue slots with (no-load fused runs: 167 cycles per
+// 256x256x16 MMA with a reducer on that sub-partition, 153 without), so from
+// 3 communication warps on the W loader, which mostly waits, takes warp 9.
+__host__ __device__ constexpr int w_loader_warp(int comm_warps) {
+  return kGemmWarps + (comm_warps >= 3 ? 3 : comm_warps);
 }
-constexpr int kSkippedWarp = kGemmWarps + 3;  // on the MMA warp's sub-partition
+__host__ __device__ constexpr int cta_warps(int comm_warps) { return kGemmWarps + 1 + comm_warps; }
 
 // Epilogue buffers: each epilogue warp stages 32 rows x 64 columns of bf16
 // (4 KiB, 128-byte swizzle) in shared memory for a TMA store, two buffers
@@ -142,6 +149,12 @@ struct GemmParams {
   // (dims {K, M, 8}; rank r's copy of every shard).  Kr is then the full K and
   // N the rank's N/8 columns.
   CUtensorMap tmap_g;
+  // W again as 4-D {64 columns, rows, column blocks of 64, 8 ranks}, box {64,
+  // 64, columns per CTA / 64, 1}: a CTA's whole stage of W in one copy
+  // instead of one per 64-column block.  Set (w4 = 1) when the W rows hold a
+  // whole number of 64-column blocks.
+  CUtensorMap tmap_w4;
+  int w4;
   const uint16_t* ag_src;  // input row shards, [8][M/8][K]
   uint16_t* gather;        // gather buffers, [8][M][K]
   uint32_t* ag_flags;      // copied chunks of shard s in rank r's buffer: ag_flags[(r*8+s)*kFlagStride]
@@ -624,7 +637,8 @@ __device__ __forceinline__ bool wait_shards(const GemmParams& p, int r, int row_
 // no tile waits for a CTA that is not running) and hands each tile index to
 // every consumer through a small ring in shared memory, mirrored into the
 // other CTAs of the cluster.  Consumers: the MMA thread of each MMA leader,
-// the 4 epilogue warps of each CTA and the TMA thread of every other CTA.
+// the 4 epilogue warps and the W loader of each CTA, and the A loader of
+// every other CTA.
 // Index -1 ends the stream.  The copies in the other CTAs are written with
 // st.async, which completes their full barrier's transaction bytes, and
 // every signal is a CTA-scope arrive: no thread waits on a cluster fence.
@@ -632,7 +646,7 @@ template <int kCtas>
 struct TileRing {
   static constexpr int kDepth = 4;
   static constexpr uint32_t kConsumers =
-      kCtas == 1 ? 1 + kEpiWarps : 2 + 2 * kEpiWarps;
+      kCtas == 1 ? 2 + kEpiWarps : 4 + 2 * kEpiWarps;
   uint32_t slots;   // shared address of int32 slot[kDepth]
   uint32_t full;    // shared address of mbarrier full[kDepth]
   uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in CTA 0)
@@ -677,8 +691,8 @@ struct TileRing {
 // The persistent GEMM kernel.  kKind adds the fused communication role (see
 // Kind); kCtas selects the tile shape (see TileCfg).
 template <int kKind, int kCtas>
-__global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_warps(kMaxReducerWarps)),
-                                  1) gemm_rs_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxReducerWarps), 1)
+    gemm_rs_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool kFused = kKind == kKindRS;  // reduce-scatter (or all-reduce) fused
   constexpr bool kAG = kKind == kKindAG;     // all-gather fused
   using C = TileCfg<kKind, kCtas>;
@@ -715,8 +729,9 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      // the MMA leader's expect-tx arrival (+ the bytes landing in its pair)
-      mbar_init(bar_full + 8 * s, 1);
+      // the MMA leader's two loaders' expect-tx arrivals (+ the bytes landing
+      // in its pair)
+      mbar_init(bar_full + 8 * s, 2);
       // one MMA commit frees the stage
       mbar_init(bar_empty + 8 * s, 1);
     }
@@ -734,7 +749,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
     fence_mbar_init();
     fence_proxy_async_shared();
     tma_prefetch_desc(&p.tmap_a);
-    tma_prefetch_desc(&p.tmap_b);
+    tma_prefetch_desc(p.w4 ? &p.tmap_w4 : &p.tmap_b);
     if (kAG) tma_prefetch_desc(&p.tmap_g);
   }
   if (warp == 1) {
@@ -752,7 +767,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
   Ring ring{ring_slots, bar_ring_full, bar_ring_empty, first_cta};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ A loader
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, issued_par = 0;
@@ -781,13 +796,6 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
         if (idx < 0) break;
         const TileCoord tc = coord(idx);
         const int m0 = tc.mt * C::kTileRows + (int)cta_rank * kBM;
-        // a half-width tile is the left or right 128 of the 256 columns: each CTA
-        // loads half as many columns of W
-        const bool half_tile = tc.half >= 0;
-        const int cta_cols = (half_tile ? kBN / 2 : kBN) / kPair;
-        const int n0 = tc.nt * kBN + (half_tile ? tc.half * (kBN / 2) : 0) + (int)half * cta_cols;
-        const int nboxes = cta_cols / 64;
-        const uint32_t stage_bytes = (uint32_t)(C::kAStage + nboxes * C::kBBoxBytes);
         const CUtensorMap* amap = &p.tmap_a;
         int arow = m0;
         if constexpr (kAG) {
@@ -818,20 +826,13 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
           }
           const uint32_t fb = bar_full + 8 * stage;
           const uint32_t sa = sbase + C::kSmemA + stage * C::kAStage;
-          const uint32_t sb = sbase + C::kSmemB + stage * C::kBStage;
           if constexpr (kCtas == 1) {
-            mbar_arrive_expect_tx(fb, stage_bytes);
+            mbar_arrive_expect_tx(fb, C::kAStage);
             tma_load_3d(sa, amap, fb, kb * kBK, arow, tc.rank);
-            for (int j = 0; j < nboxes; ++j)
-              tma_load_3d(sb + j * C::kBBoxBytes, &p.tmap_b, fb, n0 + 64 * j, kb * kBK, tc.rank);
           } else {
             // both CTAs' bytes are counted on the leader's barrier
-            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * stage_bytes);
-            const uint32_t fb_leader = mapa_shared(fb, 0);
-            tma_load_3d_pair(sa, amap, fb_leader, kb * kBK, arow, tc.rank);
-            for (int j = 0; j < nboxes; ++j)
-              tma_load_3d_pair(sb + j * C::kBBoxBytes, &p.tmap_b, fb_leader, n0 + 64 * j,
-                               kb * kBK, tc.rank);
+            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * C::kAStage);
+            tma_load_3d_pair(sa, amap, mapa_shared(fb, 0), kb * kBK, arow, tc.rank);
           }
           issued_mask |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -843,7 +844,9 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
         if (!ok) break;
       }
       // Let every copy this CTA started (or expects) land before it can exit
-      // (with a 2-CTA MMA the leader's barriers also count the peer's bytes).
+      // (with a 2-CTA MMA the leader's barriers also count the peer's bytes;
+      // a stage's barrier completes only once the W loader's copies landed
+      // too, and the W loader walks the same stages).
       if (kCtas == 1 || mma_leader)
         for (int s = 0; s < C::kStages; ++s)
           if (issued_mask & (1u << s))
@@ -855,6 +858,19 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_full = idesc_bf16_f32(kBM * kPair, kBN, /*b_mn_major=*/1);
       constexpr uint32_t idesc_half = idesc_bf16_f32(kBM * kPair, kBN / 2, /*b_mn_major=*/1);
+      // Operand descriptors of stage 0, split in halves; a stage or K step
+      // only moves the start address (low half, 16-byte units), so the loop
+      // adds constants instead of rebuilding 64-bit descriptors.
+      // A: K-major rows of 128 bytes, 8-row groups 1024 bytes apart; a
+      // 16-element K step moves 32 bytes inside the swizzled row.
+      // B: N-major; 64-column boxes 8 KiB apart (leading), 8-k-row groups
+      // 1024 bytes apart (stride); a 16-row K step moves 2 KiB.
+      const uint64_t a_desc0 = smem_desc_sw128(sbase + C::kSmemA, 16, 1024);
+      const uint64_t b_desc0 = smem_desc_sw128(sbase + C::kSmemB, C::kBBoxBytes, 1024);
+      const uint32_t a_lo0 = (uint32_t)a_desc0, a_hi = (uint32_t)(a_desc0 >> 32);
+      const uint32_t b_lo0 = (uint32_t)b_desc0, b_hi = (uint32_t)(b_desc0 >> 32);
+      // order positions from here on are half-width tiles (tile_at)
+      const long long first_half = (kAG || p.ag_order) ? p.num_tiles : (long long)kWorld * p.half_region;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -877,7 +893,7 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-        const uint32_t idesc = coord(idx).half >= 0 ? idesc_half : idesc_full;
+        const uint32_t idesc = (long long)idx >= first_half ? idesc_half : idesc_full;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!bar_wait(bar_full + 8 * stage, phase, limit, cta_abort)) {
             if (!*cta_abort) {
@@ -888,18 +904,12 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sbase + C::kSmemA + stage * C::kAStage;
-          const uint32_t sb = sbase + C::kSmemB + stage * C::kBStage;
+          const uint32_t a_lo = a_lo0 + (uint32_t)stage * (uint32_t)(C::kAStage >> 4);
+          const uint32_t b_lo = b_lo0 + (uint32_t)stage * (uint32_t)(C::kBStage >> 4);
 #pragma unroll
-          for (int s = 0; s < kBK / 16; ++s) {
-            // A: K-major rows of 128 bytes, 8-row groups 1024 bytes apart; a
-            // 16-element K step moves 32 bytes inside the swizzled row.
-            const uint64_t ad = smem_desc_sw128(sa + s * 32, 16, 1024);
-            // B: N-major; 64-column boxes 8 KiB apart (leading), 8-k-row groups
-            // 1024 bytes apart (stride); a 16-row K step moves 2 KiB.
-            const uint64_t bd = smem_desc_sw128(sb + s * 2048, C::kBBoxBytes, 1024);
-            mma_bf16<kPair>(d_tmem, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-          }
+          for (int s = 0; s < kBK / 16; ++s)
+            mma_bf16<kPair>(d_tmem, desc_join(a_lo + 2u * s, a_hi), desc_join(b_lo + 128u * s, b_hi),
+                            idesc, (kb | s) != 0 ? 1u : 0u);
           // frees the smem stage (in both CTAs of the pair) when these MMAs finish
           if constexpr (kCtas == 1)
             mma_commit<1>(bar_empty + 8 * stage);
@@ -1028,9 +1038,74 @@ __global__ void __launch_bounds__(32 * (kKind == kKindGemm ? kGemmWarps : cta_wa
     __syncwarp();
     if (trace && ew == 0 && lane == 0) trace[1] = globaltimer_ns();
     if (kFused) reducer_loop(p, lane, cta_reduced, -1);  // out of tiles: help with the reduction
-  } else if (!(warp == kSkippedWarp && (int)(blockDim.x >> 5) - kGemmWarps >= 5)) {
+  } else if (warp == w_loader_warp((int)(blockDim.x >> 5) - cta_warps(0))) {
+    // ------------------------------------------------------------ W loader
+    // Walks the same tiles and stages as the A loader; each stage's barrier
+    // takes both loaders' arrivals and bytes.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      while (true) {
+        int idx = -1;
+        if (!ring.get(&idx, limit, cta_abort)) {
+          if (!*cta_abort) {
+            record_error(p, kErrPipeTimeout, kWhereTma, 0xFFFFFFFFu);
+            *cta_abort = 1;
+          }
+          break;
+        }
+        if (idx < 0) break;
+        const TileCoord tc = coord(idx);
+        // a half-width tile is the left or right 128 of the 256 columns: each
+        // CTA loads half as many columns of W
+        const bool half_tile = tc.half >= 0;
+        const int cta_cols = (half_tile ? kBN / 2 : kBN) / kPair;
+        const int n0 = tc.nt * kBN + (half_tile ? tc.half * (kBN / 2) : 0) + (int)half * cta_cols;
+        const int nboxes = cta_cols / 64;
+        const bool one_copy = p.w4 && nboxes == C::kBBoxes;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!bar_wait(bar_empty + 8 * stage, phase ^ 1u, limit, cta_abort)) {
+            if (!*cta_abort) {
+              record_error(p, kErrPipeTimeout, kWhereTma, (uint32_t)idx);
+              *cta_abort = 1;
+            }
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          const uint32_t sb = sbase + C::kSmemB + stage * C::kBStage;
+          const uint32_t bytes = (uint32_t)(nboxes * C::kBBoxBytes);
+          if constexpr (kCtas == 1) {
+            mbar_arrive_expect_tx(fb, bytes);
+            if (one_copy)
+              tma_load_4d(sb, &p.tmap_w4, fb, 0, kb * kBK, n0 >> 6, tc.rank);
+            else
+              for (int j = 0; j < nboxes; ++j)
+                tma_load_3d(sb + j * C::kBBoxBytes, &p.tmap_b, fb, n0 + 64 * j, kb * kBK, tc.rank);
+          } else {
+            if (mma_leader) mbar_arrive_expect_tx(fb, kPair * bytes);
+            const uint32_t fb_leader = mapa_shared(fb, 0);
+            if (one_copy)
+              tma_load_4d_pair(sb, &p.tmap_w4, fb_leader, 0, kb * kBK, n0 >> 6, tc.rank);
+            else
+              for (int j = 0; j < nboxes; ++j)
+                tma_load_3d_pair(sb + j * C::kBBoxBytes, &p.tmap_b, fb_leader, n0 + 64 * j,
+                                 kb * kBK, tc.rank);
+          }
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else {
     // ------------------------------------------------- reducers / copy warps
-    const int comm_idx = warp - kGemmWarps - (warp > kSkippedWarp ? 1 : 0);
+    const int wl = w_loader_warp((int)(blockDim.x >> 5) - cta_warps(0));
+    const int comm_idx = warp - kGemmWarps - (warp > wl ? 1 : 0);
     if (kFused) reducer_loop(p, lane, cta_reduced, comm_idx);
     if (kAG) copy_loop(p, lane);
   }

@@ -37,16 +37,21 @@ struct Region {
   int mt, nt;
 };
 
-// Region at order position p (0 <= p < mt_count*nt_count).
+// Region at order position p (0 <= p < mt_count*nt_count).  The plan keeps
+// every tile count below 2^30, so the divisions are 32-bit (a 64-bit division
+// is a long software routine on the GPU, paid once per tile by the threads
+// that walk the order).
 GRS_HD Region region_at(int64_t p, int mt_count, int nt_count, int band) {
-  const int64_t band_regions = (int64_t)band * nt_count;
-  const int64_t b = p / band_regions;
-  const int64_t rem = p - b * band_regions;
-  const int mt0 = (int)(b * band);
+  const uint32_t band_regions = (uint32_t)band * (uint32_t)nt_count;
+  const uint32_t pp = (uint32_t)p;
+  const uint32_t b = pp / band_regions;
+  const uint32_t rem = pp - b * band_regions;
+  const int mt0 = (int)b * band;
   const int h = (mt_count - mt0) < band ? (mt_count - mt0) : band;  // last band may be short
+  const uint32_t q = rem / (uint32_t)h;
   Region r;
-  r.nt = (int)(rem / h);
-  r.mt = mt0 + (int)(rem % h);
+  r.nt = (int)q;
+  r.mt = mt0 + (int)(rem - q * (uint32_t)h);
   return r;
 }
 
@@ -68,19 +73,20 @@ GRS_HD int64_t tiles_of(int64_t regions, int64_t half_region) {
 
 // Rank tile at order position idx (0 <= idx < tiles_of(mt_count*nt_count, half_region)).
 GRS_HD TileCoord tile_at(int64_t idx, int mt_count, int nt_count, int band, int64_t half_region) {
-  const int64_t full = (int64_t)kWorld * half_region;
-  int64_t g;
+  static_assert(kWorld == 8, "rank = low 3 bits of the order position");
+  const uint32_t i = (uint32_t)idx;
+  const uint32_t full = (uint32_t)kWorld * (uint32_t)half_region;
+  uint32_t g;
   TileCoord t;
-  if (idx < full) {
-    g = idx / kWorld;
-    t.rank = (int)(idx % kWorld);
+  if (i < full) {
+    g = i >> 3;
+    t.rank = (int)(i & 7u);
     t.half = -1;
   } else {
-    const int64_t q = idx - full;
-    g = half_region + q / (2 * kWorld);
-    const int r16 = (int)(q % (2 * kWorld));
-    t.half = r16 / kWorld;
-    t.rank = r16 % kWorld;
+    const uint32_t q = i - full;
+    g = (uint32_t)half_region + (q >> 4);
+    t.half = (int)((q >> 3) & 1u);
+    t.rank = (int)(q & 7u);
   }
   const Region r = region_at(g, mt_count, nt_count, band);
   t.mt = r.mt;
@@ -107,13 +113,14 @@ GRS_HD int64_t half_region_of(int64_t regions, int half_regions) {
 // shards (r + 1) mod 8, (r + 2) mod 8, ... in the same order.
 GRS_HD TileCoord ag_tile_at(int64_t idx, int mt_count, int nt_count, int shard_rows,
                             int tile_rows, int band) {
-  const int64_t per_rank = (int64_t)mt_count * nt_count;
+  const uint32_t per_rank = (uint32_t)mt_count * (uint32_t)nt_count;
   TileCoord t;
   t.half = -1;
-  t.rank = (int)(idx / per_rank);
-  const Region g = region_at(idx - t.rank * per_rank, mt_count, nt_count, band);
-  const int start = (int)(((int64_t)t.rank * shard_rows) / tile_rows);
-  t.mt = (int)((start + g.mt) % mt_count);
+  t.rank = (int)((uint32_t)idx / per_rank);
+  const Region g = region_at((uint32_t)idx - (uint32_t)t.rank * per_rank, mt_count, nt_count, band);
+  const int start = (int)(((uint32_t)t.rank * (uint32_t)shard_rows) / (uint32_t)tile_rows);
+  const int mt = start + g.mt;
+  t.mt = mt >= mt_count ? mt - mt_count : mt;
   t.nt = g.nt;
   return t;
 }
