@@ -125,10 +125,12 @@ typedef struct gemm_rs_desc {
   int32_t world;          /* tensor-parallel degree; must be 8 */
   int64_t M, N, K;        /* M%8 == 0, N%8 == 0, K%64 == 0 (so K/8 is a multiple of 8); 0 allowed */
   int32_t reducer_warps;  /* FUSED: reducer warps per CTA (all-gather: copy warps), 1..5;
-                             0 = default (4, or 2 when K >= 16384; all-gather 2) */
+                             0 = default (4; 5 when K <= 6144, 2 when K >= 16384;
+                             all-gather 2) */
   int32_t grid;           /* persistent CTAs; 0 = one per SM */
   int32_t band_m;         /* tile-order band height in 128-row tiles; 0 = automatic */
-  int32_t unit_rows;      /* rows per reduce item in FUSED mode: 4, 8, 16 or 32; 0 = 8 */
+  int32_t unit_rows;      /* rows per reduce item in FUSED mode: 4, 8, 16 or 32; 0 = 8
+                             (16 when K <= 6144 and M >= 2048) */
   uint64_t timeout_ns;    /* bound on every device-side wait; 0 = 2 s */
   uint32_t debug_flags;   /* GEMM_RS_DEBUG_* */
   int32_t mma_ctas;       /* CTAs of a cluster sharing one tile: 1 (128 x 256 tiles) or 2

@@ -27,6 +27,18 @@ constexpr int kDefaultReducerWarps = 4;
 constexpr int kLargeKReducerWarps = 2;
 constexpr int64_t kLargeK = 16384;
 constexpr int kDefaultCopyWarps = 2;
+// Up to K = 6144 the reduction is the larger share of the fused kernel's work
+// and falls behind the tiles: 5 reducer warps, and 16-row items from M = 2048
+// (fewer item operations), keep it closer (fused, loaders split: 2048 x 6144 x
+// 6144 131 -> 121 us, 8192 x 6144 x 6144 504 -> 447 us; M = 512: 5 warps
+// 53 -> 47 us; at K = 8192 no change on o_proj).
+constexpr int kSmallKReducerWarps = 5;
+constexpr int64_t kSmallK = 6144;
+int default_reducer_warps(const gemm_rs_desc* d) {
+  if (d->op == GEMM_RS_OP_AG) return kDefaultCopyWarps;
+  if (d->K >= kLargeK) return kLargeKReducerWarps;
+  return d->K <= kSmallK ? kSmallKReducerWarps : kDefaultReducerWarps;
+}
 // Reduce item size: small items leave less reduction in service when the
 // last tiles finish, large ones cost fewer item operations where the
 // reduction is a large share of the work.  8-row items, and 4-row items for
@@ -34,6 +46,9 @@ constexpr int kDefaultCopyWarps = 2;
 // fused 211 -> 206 us, M = 512 78 -> 72 us against 16-row items and a
 // 1-wave tail; 8192^3 at most 3% slower).
 constexpr int kDefaultUnitRows = 8;
+int default_unit_rows(const gemm_rs_desc* d) {
+  return (d->K <= kSmallK && d->M >= 2048) ? 16 : kDefaultUnitRows;
+}
 constexpr int kDefaultTailWaves = 3;
 constexpr int kDefaultMmaCtas = 2;
 constexpr int kDefaultChunks = 4;
@@ -371,10 +386,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   if (prop.sharedMemPerBlockOptin < (size_t)gemm_smem_max(pair)) return GEMM_RS_ERR_UNSUPPORTED_DEVICE;
   // reducer warps (reduce-scatter) or copy warps (all-gather: 2 keep the
   // copies ahead of the tiles with the least interference)
-  const int reducer_warps = d->reducer_warps > 0 ? d->reducer_warps
-                            : d->op == GEMM_RS_OP_AG ? kDefaultCopyWarps
-                            : d->K >= kLargeK        ? kLargeKReducerWarps
-                                                     : kDefaultReducerWarps;
+  const int reducer_warps = d->reducer_warps > 0 ? d->reducer_warps : default_reducer_warps(d);
   int grid = 0;
   rc = prepare_kernels(dev, prop.multiProcessorCount, pair, d->grid,
                        32 * cta_warps(reducer_warps), &grid);
@@ -400,7 +412,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
   h->band = d->band_m > 0 ? (d->band_m < h->mt ? d->band_m : h->mt)
                           : auto_band(d->M, d->K, h->tile_rows);
   if (h->band < 1) h->band = 1;
-  h->unit_rows = d->unit_rows > 0 ? d->unit_rows : kDefaultUnitRows;
+  h->unit_rows = d->unit_rows > 0 ? d->unit_rows : default_unit_rows(d);
   h->splits = kBM / h->unit_rows;
   h->blocks_per_region = h->tile_rows / kBM;
   const long long blocks = (long long)h->mt * h->nt * h->blocks_per_region;
@@ -496,10 +508,8 @@ int gemm_rs_tune_candidates(const gemm_rs_desc* d, gemm_rs_desc* cands, int max,
   auto resolve = [&](Knobs k) {
     Knobs r;
     r.ctas = k.ctas > 0 ? k.ctas : kDefaultMmaCtas;
-    r.warps = k.warps > 0 ? k.warps
-              : ag            ? kDefaultCopyWarps
-                              : (d->K >= kLargeK ? kLargeKReducerWarps : kDefaultReducerWarps);
-    r.units = ag ? 0 : (k.units > 0 ? k.units : kDefaultUnitRows);
+    r.warps = k.warps > 0 ? k.warps : default_reducer_warps(d);
+    r.units = ag ? 0 : (k.units > 0 ? k.units : default_unit_rows(d));
     const int tile_rows = kBM * r.ctas;
     const int mtc = (int)((d->M + tile_rows - 1) / tile_rows);
     const int ab = auto_band(d->M, d->K, tile_rows);
@@ -1213,8 +1223,15 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.nt_count = (int)nt;
     p.band = auto_band(M, K, tile_rows);
     p.num_kb = (int)((Kr + kBK - 1) / kBK);
-    p.unit_rows = kDefaultUnitRows;
-    p.splits = kBM / kDefaultUnitRows;
+    gemm_rs_desc dd;  // the default plan's reducer warps and item size for this shape
+    memset(&dd, 0, sizeof(dd));
+    dd.M = M;
+    dd.N = N;
+    dd.K = K;
+    dd.op = GEMM_RS_OP_RS;
+    const int reducers = default_reducer_warps(&dd);
+    p.unit_rows = default_unit_rows(&dd);
+    p.splits = kBM / p.unit_rows;
     p.blocks_per_region = tile_rows / kBM;
     p.tile_rows = tile_rows;
     p.half_region = (int)half_region_of(mt * nt, 0);
@@ -1224,8 +1241,8 @@ extern "C" int gemm_rs_fused_noalloc(const void* A, const void* W, void* out, in
     p.tail_region = (int)tail;
     p.num_items = items_of(blocks, p.blocks_per_region, tail, p.splits);
     p.timeout_ns = kDefaultTimeoutNs;
-    rc = launch_gemm_kernel(kDefaultMmaCtas, kKindRS, nd->grid,
-                            32 * cta_warps(kDefaultReducerWarps), p, st);
+    p.reducer_warps = reducers;
+    rc = launch_gemm_kernel(kDefaultMmaCtas, kKindRS, nd->grid, 32 * cta_warps(reducers), p, st);
     if (rc != GEMM_RS_OK) return rc;
   }
   if (error_word && cudaMemcpyAsync(error_word, ctrl + kCtrlError * kCtrlStride, sizeof(uint32_t),

@@ -195,7 +195,7 @@ def test_tune_candidates_and_their_workspace(lib, op):
     assert (c0.mma_ctas, c0.reducer_warps, c0.unit_rows, c0.band_m, c0.tail_waves) == (0, 0, 0, 0, 0)
     def resolved(c):
         ctas = c.mma_ctas or 2
-        return (ctas, c.reducer_warps or (4 if op == 0 else 2),  # K = 4096 < 16384
+        return (ctas, c.reducer_warps or (5 if op == 0 else 2),  # K = 4096 <= 6144: 5 reducers
                 (c.unit_rows or 8) if op == 0 else 0, c.band_m or (4 if ctas == 2 else 8),
                 (c.tail_waves or 3) if op == 0 else 0,
                 max(c.half_regions, 0) if (op == 0 and ctas == 2) else 0)
