@@ -141,7 +141,7 @@ constexpr int kFlagStride = 32;   // words: one 128-byte line per block count
 constexpr int kQueueStride = 4;   // 8-byte words per item's debug stamps (one 32-byte sector)
 enum ErrBits : uint32_t { kErrFlagTimeout = 1u, kErrPipeTimeout = 2u, kErrIncomplete = 4u };
 enum ErrWhere : uint32_t {
-  kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereReducer = 4, kWhereShard = 5
+  kWhereTma = 1, kWhereMma = 2, kWhereEpi = 3, kWhereReducer = 4, kWhereShard = 5, kWhereRing = 6
 };
 
 struct GemmParams {
@@ -383,7 +383,7 @@ __device__ __forceinline__ int item_pop(const GemmParams& p, int lane, Item* it,
 // lane, then the rank-order sums and the stores.
 template <int R>
 __device__ __forceinline__ void reduce_rows(const GemmParams& p, size_t plane, int row, int col,
-                                            bool active, bool drop) {
+                                            bool active, bool drop, int lane, int col0) {
   const size_t off = (size_t)row * p.N + col;
   if (active) {
     uint4 v[R][kWorld];
@@ -402,12 +402,17 @@ __device__ __forceinline__ void reduce_rows(const GemmParams& p, size_t plane, i
   }
   if (p.staging_in_l2) {
     __syncwarp();  // every lane has consumed its loads (its stores depend on them)
+    // R rows x 8 ranks x 4 lines of 128 bytes: spread over the 32 lanes (R
+    // lines each) rather than issued by the 4 lanes that start a line, which
+    // serialised 8 * R discards on each of them
     if (drop) {
 #pragma unroll
-      for (int i = 0; i < R; ++i)
-#pragma unroll
-        for (int r = 0; r < kWorld; ++r)
-          discard_l2_line(p.stage + r * plane + off + (size_t)i * p.N);
+      for (int i = 0; i < R; ++i) {
+        const int line = lane + 32 * i;       // (rank, row, 128-byte segment) of the R rows
+        const int seg = line & 3, r = (line >> 2) & 7, ri = line >> 5;
+        if (col0 + seg * 64 < p.N)
+          discard_l2_line(p.stage + r * plane + (size_t)(row + ri) * p.N + col0 + seg * 64);
+      }
     }
   }
 }
@@ -426,17 +431,18 @@ __device__ __forceinline__ void reduce_item(const GemmParams& p, const Item& it,
   if (row_begin >= p.M) return;  // rows of a ragged last tile that do not exist
   int row_end = row_begin + rows;
   if (row_end > p.M) row_end = p.M;
-  const int col = nt * kBN + lane * 8;
+  const int col0 = nt * kBN;
+  const int col = col0 + lane * 8;
   const bool active = col < p.N;
-  const bool drop = p.staging_in_l2 && active && (lane & 7) == 0;
+  const bool drop = p.staging_in_l2;
   int row = row_begin;
 #pragma unroll 1
-  for (; row + 3 < row_end; row += 4) reduce_rows<4>(p, plane, row, col, active, drop);
+  for (; row + 3 < row_end; row += 4) reduce_rows<4>(p, plane, row, col, active, drop, lane, col0);
   if (row + 1 < row_end) {
-    reduce_rows<2>(p, plane, row, col, active, drop);
+    reduce_rows<2>(p, plane, row, col, active, drop, lane, col0);
     row += 2;
   }
-  if (row < row_end) reduce_rows<1>(p, plane, row, col, active, drop);
+  if (row < row_end) reduce_rows<1>(p, plane, row, col, active, drop, lane, col0);
 }
 
 // Adaptive reducer share (mKernel page, section 3.2: a controller estimates
@@ -651,15 +657,22 @@ __device__ __forceinline__ bool wait_shards(const GemmParams& p, int r, int row_
 template <int kCtas>
 struct TileRing {
   static constexpr int kDepth = 4;
-  static constexpr uint32_t kConsumers =
-      kCtas == 1 ? 2 + kEpiWarps : 4 + 2 * kEpiWarps;
+  // Readers of a slot in each CTA: the W loader, the epilogue warps, and the
+  // MMA issuer in CTA 0 (whose A loader writes the slots) or the A loader in
+  // the other CTA.
+  static constexpr uint32_t kLocalConsumers = 2 + kEpiWarps;
   uint32_t slots;   // shared address of int32 slot[kDepth]
   uint32_t full;    // shared address of mbarrier full[kDepth]
-  uint32_t empty;   // shared address of mbarrier empty[kDepth] (used in CTA 0)
+  uint32_t empty;   // shared address of mbarrier empty[kDepth]
   bool owner;       // this CTA is CTA 0, which claims the tiles
   int slot = 0;
   uint32_t phase = 0;
 
+  // Arrivals that free a slot: the CTA's own readers, and in CTA 0 of a pair
+  // one more, forwarded by the other CTA once all of its readers are done.
+  static __device__ __forceinline__ uint32_t empty_count(bool is_owner) {
+    return kLocalConsumers + ((kCtas > 1 && is_owner) ? 1u : 0u);
+  }
   __device__ __forceinline__ void advance() {
     if (++slot == kDepth) {
       slot = 0;
@@ -668,7 +681,8 @@ struct TileRing {
   }
   // Producer (CTA 0's TMA thread): publish the next claimed tile, or -1.
   __device__ __forceinline__ bool put(int tile, uint64_t limit, volatile uint32_t* abort) {
-    if (!bar_wait(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
+    // cluster-scope acquire: pairs with the other CTA's forwarded release
+    if (!bar_wait<(kCtas > 1)>(empty + 8 * slot, phase ^ 1u, limit, abort)) return false;
     st_shared_u32(slots + 4 * slot, (uint32_t)tile);
     mbar_arrive(full + 8 * slot);
 #pragma unroll
@@ -681,15 +695,34 @@ struct TileRing {
     return true;
   }
   // Consumer: next tile index (-1 at the end); false if the wait gave up.
+  // The arrival is local (CTA-scope release after the read) in every CTA.
+  // In the other CTA the slot is written by CTA 0's st.async, and the slot's
+  // barrier there completes only once those 4 bytes have landed in this CTA's
+  // shared memory (its transaction count), so the wait is a local one.
   __device__ __forceinline__ bool get(int* tile, uint64_t limit, volatile uint32_t* abort) {
     if (!bar_wait(full + 8 * slot, phase, limit, abort)) return false;
     *tile = (int)ld_shared_u32(slots + 4 * slot);
-    if (kCtas == 1 || owner)
-      mbar_arrive(empty + 8 * slot);
-    else
-      mbar_arrive_remote(mapa_shared(empty + 8 * slot, 0));
+    mbar_arrive(empty + 8 * slot);
     advance();
     return true;
+  }
+  // Forwarder (one otherwise idle thread of the other CTA): once every reader
+  // of this CTA has arrived on a slot's local barrier, pass one arrival on to
+  // CTA 0's barrier of that slot, with release at cluster scope, so that all
+  // those reads are performed before CTA 0 may rewrite the slot.  (A remote
+  // arrival of CTA scope from each reader let the rewrite overtake a read now
+  // and then: a reader then took a tile twice and skipped another.  A
+  // cluster-scope release from each reader closed that too, but cost 2-7% of
+  // the GEMM's time.)  Ends after forwarding the -1 slot.
+  __device__ __forceinline__ bool forward(uint64_t limit, volatile uint32_t* abort) {
+    while (true) {
+      if (!bar_wait<true>(full + 8 * slot, phase, limit, abort)) return false;
+      const int tile = (int)ld_shared_u32(slots + 4 * slot);
+      if (!bar_wait(empty + 8 * slot, phase, limit, abort)) return false;
+      mbar_arrive_remote_release_cluster(mapa_shared(empty + 8 * slot, 0));
+      advance();
+      if (tile < 0) return true;
+    }
   }
 };
 
@@ -748,7 +781,7 @@ __global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxRe
     mbar_init(bar_drain, 1);
     for (int s = 0; s < Ring::kDepth; ++s) {
       mbar_init(bar_ring_full + 8 * s, 1);
-      mbar_init(bar_ring_empty + 8 * s, Ring::kConsumers);
+      mbar_init(bar_ring_empty + 8 * s, Ring::empty_count(first_cta));
     }
     *cta_abort = 0;
     *cta_reduced = 0;
@@ -942,8 +975,14 @@ __global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxRe
       bar_wait(bar_drain, 0, limit, cta_abort);
       if (trace) trace[2] = globaltimer_ns();
     }
+    if constexpr (kCtas > 1) {
+      if (lane == 0 && !first_cta && !ring.forward(limit, cta_abort) && !*cta_abort) {
+        record_error(p, kErrPipeTimeout, kWhereRing, 0xFFFFFFFFu);
+        *cta_abort = 1;
+      }
+    }
     __syncwarp();
-    if (kFused && mma_leader) reducer_loop(p, lane, cta_reduced, -1);
+    if (kFused) reducer_loop(p, lane, cta_reduced, -1);  // MMA issuer or forwarder: out of tiles
   } else if (warp < kGemmWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;     // TMEM lane quadrant this warp can read

@@ -63,6 +63,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
+// Remote arrive with release at cluster scope: the arriving thread's earlier
+// memory operations (e.g. its read of a shared-memory slot that the other CTA
+// will overwrite once every arrival is in) are performed before the arrival
+// is visible in the other CTA.
+__device__ __forceinline__ void mbar_arrive_remote_release_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
 // Remote arrive that also expects `bytes` more transaction bytes this phase.
 __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
