@@ -664,7 +664,7 @@ def run_sweep(args, local):
             t_def = metrics.median([v for k, v in tt if k == "default"])
             t_tun = metrics.median([v for k, v in tt if k == "tuned"])
             knobs = {k: best[k] for k in ("mma_ctas", "reducer_warps", "unit_rows", "band_m", "tail_waves",
-                                          "half_regions")}
+                                          "half_regions", "copy_engines")}
             tuned = {"plan": knobs, "t_fused_tuned_us": t_tun * 1e6, "t_fused_default_us": t_def * 1e6,
                      "tuner_best_us": best_us, "candidates": len(table)}
             tplan.close()

@@ -155,6 +155,16 @@ typedef struct gemm_rs_desc {
                              columns), so the final wave is shorter; 0 or -1 = none (the
                              default), 1..4096 (clamped to the regions there are).  Every mode
                              uses the same tiles, and the results do not depend on it */
+  int32_t copy_engines;   /* all-gather + GEMM, FUSED: what moves the 7 other ranks' row
+                             shards into each rank's gather buffer while the tiles run.
+                             -1 = copy warps inside the fused kernel (reducer_warps of them);
+                             1..4 = the GPU's copy engines: one device-to-device copy per
+                             (rank, shard) on that many side streams of the plan, each
+                             followed on its stream by a write of that shard's count (the
+                             value the tiles wait for), and no copy warps in the kernel; the
+                             side streams start after the work already queued on the run's
+                             stream, and that stream waits for them after the kernel.
+                             0 = default (-1).  Ignored by the row-parallel layer */
 } gemm_rs_desc;
 
 typedef struct gemm_rs_plan_s* gemm_rs_t;
@@ -185,6 +195,8 @@ typedef struct gemm_rs_info {
   int64_t queue_offset;   /* byte offset of the reduce items' debug stamps in the workspace */
   int64_t half_region;    /* first region (in tile order) computed in half-width tiles; the
                              region count if none */
+  int32_t copy_engines;   /* AG: side streams of copy-engine copies in FUSED runs; -1 = copy
+                             warps; 0 for the row-parallel layer */
 } gemm_rs_info;
 
 /*

@@ -54,6 +54,8 @@ constexpr int kDefaultMmaCtas = 2;
 constexpr int kDefaultChunks = 4;
 constexpr int kMaxChunks = 64;
 constexpr long long kCopyChunk = 32768;  // elements per all-gather copy item (64 KiB)
+constexpr int kMaxCopyStreams = 4;       // all-gather: side streams of copy-engine copies
+constexpr int kDefaultCopyEngines = -1;  // all-gather: copy warps in the fused kernel
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -104,6 +106,7 @@ int check_desc(const gemm_rs_desc* d) {
   if (d->adaptive != 0 && d->adaptive != 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->tail_waves < 0 || d->tail_waves > 64) return GEMM_RS_ERR_INVALID_ARG;
   if (d->half_regions < -1 || d->half_regions > 4096) return GEMM_RS_ERR_INVALID_ARG;
+  if (d->copy_engines < -1 || d->copy_engines > kMaxCopyStreams) return GEMM_RS_ERR_INVALID_ARG;
   if (d->op == GEMM_RS_OP_AG && d->replicas > 1) return GEMM_RS_ERR_INVALID_ARG;
   if (d->M < 0 || d->N < 0 || d->K < 0) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
   if (d->M % 8 || d->N % 8 || d->K % 64) return GEMM_RS_ERR_UNSUPPORTED_SHAPE;
@@ -131,6 +134,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Stream-ordered 32-bit write (the all-gather's copy-engine path publishes a
+// copied shard's count with it, after the copy on the same stream).
+PFN_cuStreamWriteValue32_v11070 write_value_fn() {
+  static PFN_cuStreamWriteValue32_v11070 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &ptr, 11070, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuStreamWriteValue32_v11070>(ptr);
   }
   return fn;
 }
@@ -318,6 +336,11 @@ struct gemm_rs_plan_s {
   bool ag = false;
   int shard_rows = 0, ag_direct = 0, chunks_per_shard = 0, first_round = 0;
   long long copy_items = 0;
+  // FUSED all-gather by copy engines: side streams and events (created on first use)
+  int copy_engines = 0;
+  cudaStream_t copy_st[kMaxCopyStreams] = {};
+  cudaEvent_t copy_fork = nullptr;
+  cudaEvent_t copy_join[kMaxCopyStreams] = {};
 };
 
 extern "C" {
@@ -445,6 +468,7 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
     h->chunks_per_shard = (int)((shard_elems + kCopyChunk - 1) / kCopyChunk);
     h->first_round = h->ag_direct;
     h->copy_items = (long long)(kWorld - h->first_round) * kWorld * h->chunks_per_shard;
+    h->copy_engines = d->copy_engines != 0 ? d->copy_engines : kDefaultCopyEngines;
     h->items = 0;
     h->tail_region = 0;
     h->chunks = 0;
@@ -486,7 +510,9 @@ int gemm_rs_get_info(gemm_rs_t h, gemm_rs_info* info) {
     info->launches[GEMM_RS_RS_ONLY] = empty || h->d.K == 0 ? 0 : 1;  // the gather kernel
     info->launches[GEMM_RS_CHUNKED] = 0;                           // not defined
     info->ag_direct = h->ag_direct;
-    info->copy_items = h->copy_items;
+    info->copy_items = h->copy_engines > 0 ? 0 : h->copy_items;
+    info->copy_engines = h->copy_engines;
+    if (h->copy_engines > 0) info->threads_fused = 32 * cta_warps(0);
   }
   info->mma_ctas = h->pair;
   info->tile_rows = h->tile_rows;
@@ -689,6 +715,11 @@ int gemm_rs_destroy(gemm_rs_t h) {
     for (int c = 0; c < kMaxChunks; ++c)
       if (h->ev_chunk[c]) cudaEventDestroy(h->ev_chunk[c]);
   }
+  for (int e = 0; e < kMaxCopyStreams; ++e) {
+    if (h->copy_st[e]) cudaStreamDestroy(h->copy_st[e]);
+    if (h->copy_join[e]) cudaEventDestroy(h->copy_join[e]);
+  }
+  if (h->copy_fork) cudaEventDestroy(h->copy_fork);
   delete h;
   return GEMM_RS_OK;
 }
@@ -798,6 +829,71 @@ static int launch_gather(gemm_rs_t h, const void* A, void* gather, cudaStream_t 
   return cudaGetLastError() == cudaSuccess ? GEMM_RS_OK : GEMM_RS_ERR_CUDA;
 }
 
+// FUSED all-gather by copy engines: fork the plan's side streams off st, then
+// per rank (in the order the tiles take the ranks) and per shard (in the
+// order the rank's tiles read them: its own shard + 1, + 2, ...) one
+// device-to-device copy into the rank's gather buffer, followed on the same
+// stream by a write of `target` to that (rank, shard)'s count.  The copies
+// run on the copy engines, beside the kernel that holds the SMs.
+static int issue_engine_copies(gemm_rs_t h, const void* A, uint8_t* wsb, uint32_t target,
+                               cudaStream_t st) {
+  const int E = h->copy_engines;
+  if (!h->copy_fork) {  // all or nothing: a failed setup leaves no stream behind
+    bool ok = cudaEventCreateWithFlags(&h->copy_fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int e = 0; ok && e < E; ++e)
+      ok = cudaStreamCreateWithFlags(&h->copy_st[e], cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h->copy_join[e], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      for (int e = 0; e < kMaxCopyStreams; ++e) {
+        if (h->copy_st[e]) cudaStreamDestroy(h->copy_st[e]);
+        if (h->copy_join[e]) cudaEventDestroy(h->copy_join[e]);
+        h->copy_st[e] = nullptr;
+        h->copy_join[e] = nullptr;
+      }
+      if (h->copy_fork) cudaEventDestroy(h->copy_fork);
+      h->copy_fork = nullptr;
+      cudaGetLastError();
+      return GEMM_RS_ERR_CUDA;
+    }
+  }
+  auto write_value = write_value_fn();
+  if (!write_value) return GEMM_RS_ERR_CUDA;
+  if (cudaEventRecord(h->copy_fork, st) != cudaSuccess) return GEMM_RS_ERR_CUDA;
+  for (int e = 0; e < E; ++e)
+    if (cudaStreamWaitEvent(h->copy_st[e], h->copy_fork, 0) != cudaSuccess) return GEMM_RS_ERR_CUDA;
+  const size_t row_bytes = (size_t)h->d.K * 2;
+  const size_t shard_bytes = (size_t)h->shard_rows * row_bytes;
+  const uint8_t* src = static_cast<const uint8_t*>(A);
+  uint32_t* counts = reinterpret_cast<uint32_t*>(wsb + h->lay.flags_off);
+  int n = 0;
+  for (int r = 0; r < kWorld; ++r)
+    for (int k = h->first_round; k < kWorld; ++k) {
+      const int s = (r + k) % kWorld;
+      cudaStream_t cs = h->copy_st[n++ % E];
+      uint8_t* dst = wsb + ((size_t)r * (size_t)h->d.M + (size_t)s * h->shard_rows) * row_bytes;
+      if (cudaMemcpyAsync(dst, src + (size_t)s * shard_bytes, shard_bytes, cudaMemcpyDeviceToDevice,
+                          cs) != cudaSuccess)
+        return GEMM_RS_ERR_CUDA;
+      // debug: the first (rank, shard) is copied but never published
+      if ((h->d.debug_flags & GEMM_RS_DEBUG_SKIP_ONE_FLAG) && r == 0 && k == h->first_round) continue;
+      const CUdeviceptr count = reinterpret_cast<CUdeviceptr>(counts + (size_t)(r * kWorld + s) * kFlagStride);
+      if (write_value(reinterpret_cast<CUstream>(cs), count, target, CU_STREAM_WRITE_VALUE_DEFAULT) !=
+          CUDA_SUCCESS)
+        return GEMM_RS_ERR_CUDA;
+    }
+  return GEMM_RS_OK;
+}
+
+// st waits for the side streams' copies and count writes.
+static int join_engine_copies(gemm_rs_t h, cudaStream_t st) {
+  if (!h->copy_fork) return GEMM_RS_OK;  // never set up: nothing was queued on a side stream
+  for (int e = 0; e < h->copy_engines; ++e)
+    if (cudaEventRecord(h->copy_join[e], h->copy_st[e]) != cudaSuccess ||
+        cudaStreamWaitEvent(st, h->copy_join[e], 0) != cudaSuccess)
+      return GEMM_RS_ERR_CUDA;
+  return GEMM_RS_OK;
+}
+
 static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out, void* ws,
                   cudaStream_t st) {
   const gemm_rs_desc& d = h->d;
@@ -885,6 +981,14 @@ static int run_ag(gemm_rs_t h, int mode, const void* A, const void* W, void* out
   if (fused) {
     h->epoch += 1;
     p.ag_target = (uint32_t)h->chunks_per_shard * h->epoch;  // every copied (rank, shard)
+    if (h->copy_engines > 0) {  // copies by the copy engines; the kernel has no copy warps
+      p.copy_items = 0;
+      int rc = issue_engine_copies(h, A, wsb, p.ag_target, st);
+      if (rc == GEMM_RS_OK)
+        rc = launch_gemm_kernel(h->pair, kKindAG, h->grid, 32 * cta_warps(0), p, st);
+      const int rj = join_engine_copies(h, st);  // also after a failed launch: st follows the copies
+      return rc != GEMM_RS_OK ? rc : rj;
+    }
     return launch_gemm_kernel(h->pair, kKindAG, h->grid, 32 * cta_warps(h->reducer_warps),
                               p, st);
   }

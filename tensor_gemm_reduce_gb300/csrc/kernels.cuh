@@ -652,8 +652,9 @@ __device__ __forceinline__ bool wait_shards(const GemmParams& p, int r, int row_
 // the 4 epilogue warps and the W loader of each CTA, and the A loader of
 // every other CTA.
 // Index -1 ends the stream.  The copies in the other CTAs are written with
-// st.async, which completes their full barrier's transaction bytes, and
-// every signal is a CTA-scope arrive: no thread waits on a cluster fence.
+// st.async, which completes their full barrier's transaction bytes; readers
+// arrive on their own CTA's barrier, and one thread of each other CTA passes
+// the slot's release on to CTA 0 at cluster scope (TileRing::forward).
 template <int kCtas>
 struct TileRing {
   static constexpr int kDepth = 4;

@@ -66,6 +66,7 @@ class gemm_rs_desc(ctypes.Structure):
         ("adaptive", ctypes.c_int32),
         ("tail_waves", ctypes.c_int32),
         ("half_regions", ctypes.c_int32),
+        ("copy_engines", ctypes.c_int32),
     ]
 
 
@@ -95,6 +96,7 @@ class gemm_rs_info(ctypes.Structure):
         ("copy_items", ctypes.c_int64),
         ("queue_offset", ctypes.c_int64),
         ("half_region", ctypes.c_int64),
+        ("copy_engines", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -180,9 +182,10 @@ def strerror(code: int) -> str:
 
 def _desc(M, N, K, reducer_warps=0, grid=0, band_m=0, unit_rows=0, timeout_ns=0, debug_flags=0,
           mma_ctas=0, chunks=0, replicas=0, op=OP_RS, adaptive=0, tail_waves=0, half_regions=0,
-          world=WORLD):
+          copy_engines=0, world=WORLD):
     return gemm_rs_desc(world, M, N, K, reducer_warps, grid, band_m, unit_rows, timeout_ns,
-                        debug_flags, mma_ctas, chunks, replicas, op, adaptive, tail_waves, half_regions)
+                        debug_flags, mma_ctas, chunks, replicas, op, adaptive, tail_waves, half_regions,
+                        copy_engines)
 
 
 # ----------------------------------------------------------------------------
@@ -263,13 +266,14 @@ class Plan:
     def __init__(self, M: int, N: int, K: int, *, reducer_warps: int = 0, grid: int = 0,
                  band_m: int = 0, unit_rows: int = 0, timeout_ns: int = 0, debug_flags: int = 0,
                  mma_ctas: int = 0, chunks: int = 0, replicas: int = 0, op: int = OP_RS,
-                 adaptive: int = 0, tail_waves: int = 0, half_regions: int = 0):
+                 adaptive: int = 0, tail_waves: int = 0, half_regions: int = 0,
+                 copy_engines: int = 0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.replicas = max(1, int(replicas))
         self.op = int(op)
         self.desc = _desc(self.M, self.N, self.K, reducer_warps, grid, band_m, unit_rows,
                           timeout_ns, debug_flags, mma_ctas, chunks, replicas, op, adaptive,
-                          tail_waves, half_regions)
+                          tail_waves, half_regions, copy_engines)
         self._h, self.workspace_bytes = gemm_rs_create(self.desc)
 
     @property
@@ -424,7 +428,8 @@ def gemm_rs(A, W, out=None, workspace=None, mode: int = FUSED, plan: Optional[Pl
 
 TUNE_MAX = 32
 _DESC_KW = ("reducer_warps", "grid", "band_m", "unit_rows", "timeout_ns", "debug_flags",
-            "mma_ctas", "chunks", "replicas", "op", "adaptive", "tail_waves", "half_regions")
+            "mma_ctas", "chunks", "replicas", "op", "adaptive", "tail_waves", "half_regions",
+            "copy_engines")
 
 
 def tune_candidates(desc: gemm_rs_desc):

@@ -66,6 +66,8 @@ def _create(**kw):
     (dict(op=2), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=G.OP_AG, replicas=8), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(op=G.OP_AG, N=264), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
+    (dict(op=G.OP_AG, copy_engines=-2), G.GEMM_RS_ERR_INVALID_ARG),
+    (dict(op=G.OP_AG, copy_engines=5), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(replicas=-1), G.GEMM_RS_ERR_INVALID_ARG),
     (dict(M=100), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),
     (dict(N=12), G.GEMM_RS_ERR_UNSUPPORTED_SHAPE),

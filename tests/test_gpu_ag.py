@@ -93,6 +93,12 @@ def test_tiny_workload():
     (2048, 2560, 1024, dict(reducer_warps=5), True),
     (2048, 4096, 512, dict(grid=8), True),   # 16 tiles per rank >= 2 waves of 4 clusters: paced copies
     (1024, 4096, 512, dict(grid=4, mma_ctas=1), True),  # paced, 1-CTA tiles
+    # shards moved by the copy engines on 1..4 side streams, no copy warps
+    (2048, 2560, 1024, dict(copy_engines=1), True),
+    (2048, 2560, 1024, dict(copy_engines=4, grid=6), True),
+    (1024, 1024, 512, dict(mma_ctas=1, copy_engines=2), True),
+    (392, 1536, 1600, dict(copy_engines=3), False),       # own shard copied too
+    (8, 512, 64, dict(copy_engines=2), False),
 ])
 def test_shapes_and_plans(M, N, K, kw, direct):
     A, W = workloads.make_shape_inputs(M, N, K, seed=M + 2 * N + K, op="ag")
@@ -100,6 +106,10 @@ def test_shapes_and_plans(M, N, K, kw, direct):
     assert bool(c.plan.info.ag_direct) == direct
     n_rounds = 7 if direct else 8
     assert c.plan.info.copy_items % (8 * n_rounds) == 0
+    engines = kw.get("copy_engines", 0)
+    assert c.plan.info.copy_engines == (engines or -1)
+    if engines > 0:  # the fused kernel runs without copy warps
+        assert c.plan.info.copy_items == 0 and c.plan.info.threads_fused == c.plan.info.threads_gemm
 
 
 def test_zero_k_and_host_copies():
@@ -121,14 +131,16 @@ def test_zero_k_and_host_copies():
     assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16).cpu())
 
 
-def test_unpublished_copy_times_out_and_recovers():
-    """The first copy item is never published: the tiles that need its shard
-    give up after 20 ms, the status says TIMEOUT, and the next run is clean."""
+@pytest.mark.parametrize("engines", [0, 2])
+def test_unpublished_copy_times_out_and_recovers(engines):
+    """The first copy (a copy warp's item, or a copy engine's shard) is never
+    published: the tiles that need its shard give up after 20 ms, the status
+    says TIMEOUT, and the next run is clean."""
     A, W = workloads.make_shape_inputs(1024, 2048, 1024, seed=72, op="ag")
-    bad = AGCase(A, W, timeout_ns=20_000_000, debug_flags=G.DEBUG_SKIP_ONE_FLAG)
+    bad = AGCase(A, W, timeout_ns=20_000_000, debug_flags=G.DEBUG_SKIP_ONE_FLAG, copy_engines=engines)
     bad.plan.run(bad.A, bad.W, bad.out, bad.ws, G.FUSED)
     assert bad.plan.status() == G.GEMM_RS_ERR_TIMEOUT
-    good = AGCase(A, W)
+    good = AGCase(A, W, copy_engines=engines)
     C, _ = oracle.ag_gemm(A, W)
     out = to_host_values(good.run(G.FUSED, poison=True))
     assert oracle.err_vs_oracle(out.reshape(-1, out.shape[-1]), C.reshape(-1, C.shape[-1])) <= TOL
