@@ -800,6 +800,14 @@ __global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxRe
   __syncthreads();
   if constexpr (kCtas > 1) cluster_sync();  // every CTA's barriers exist before any remote use
   tc_fence_after();
+  // The set-up above touches only this CTA's own shared memory and TMEM, so
+  // with programmatic dependent launch it overlaps the previous grid's last
+  // CTAs; nothing below runs before that grid (which may use the same
+  // workspace, counts and output) has completed.  Each CTA lets the next grid
+  // be scheduled as soon as it is running: that grid's CTAs then take the SMs
+  // this grid leaves, and none of this grid's CTAs waits for an SM.
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   unsigned long long* trace =
       (p.trace && blockIdx.x < kMaxTraceCtas) ? p.trace + blockIdx.x * kTraceWords : nullptr;
@@ -1229,7 +1237,6 @@ __global__ void __launch_bounds__(256) rs_reduce_kernel(const uint16_t* __restri
 }
 
 
-// Zero fill (empty contraction, K = 0): n16 16-byte vectors.
 // Standalone all-gather of the unfused path: every rank's gather buffer gets
 // all 8 row shards, its own included.  Rank r's buffer [M][K] is the 8 shards
 // one after the other, which is the input's own layout, so it is a copy of
@@ -1247,6 +1254,7 @@ __global__ void __launch_bounds__(256) ag_gather_kernel(const uint16_t* __restri
     d[v] = __ldg(s + v % per_rank);
 }
 
+// Zero fill (empty contraction, K = 0): n16 16-byte vectors.
 __global__ void __launch_bounds__(256) zero_fill_kernel(uint4* __restrict__ p, long long n16) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
