@@ -270,6 +270,62 @@ def test_repeated_runs_reuse_flags():
     assert_parity(to_host_values(first), out, None)
 
 
+@pytest.mark.parametrize("kw", [{}, dict(mma_ctas=1), dict(grid=4)])
+def test_back_to_back_runs_with_changing_inputs(kw):
+    """Fused runs queued back to back on one stream and one workspace, with no
+    host sync or memset between them (so each launch's set-up overlaps the
+    previous grid), alternating two inputs and four output buffers, then the
+    other modes behind them: every output equals its own input's UNFUSED
+    result bit for bit, and the status stays OK."""
+    M, N, K = 640, 1024, 2048
+    A1, W1 = workloads.make_shape_inputs(M, N, K, seed=31)
+    A2, W2 = workloads.make_shape_inputs(M, N, K, seed=32)
+    c = Case(A1, W1, **kw)
+    ins = [(c.A, c.W), (to_dev(A2), to_dev(W2))]
+    refs = []
+    for a, w in ins:
+        c.plan.run(a, w, c.out, c.ws, G.UNFUSED)
+        torch.cuda.synchronize()
+        refs.append(c.out.clone())
+    outs = [torch.full_like(c.out, float("nan")) for _ in range(6)]
+    modes = [G.FUSED, G.FUSED, G.FUSED, G.FUSED, G.GEMM_ONLY, G.FUSED]
+    for i, (o, mode) in enumerate(zip(outs, modes)):
+        a, w = ins[i % 2]
+        c.plan.run(a, w, o, c.ws, mode)
+    torch.cuda.synchronize()
+    assert c.plan.status() == G.GEMM_RS_OK
+    for i, (o, mode) in enumerate(zip(outs, modes)):
+        if mode == G.FUSED:
+            assert torch.equal(o.view(torch.int16), refs[i % 2].view(torch.int16)), i
+
+
+def test_back_to_back_layers_share_a_stream():
+    """A reduce-scatter layer and an all-gather layer queued alternately on one
+    stream with their own workspaces, no sync between: both stay exact."""
+    M, N, K = 1024, 2048, 1024
+    A, W = workloads.make_shape_inputs(M, N, K, seed=41)
+    A_ag, W_ag = workloads.make_shape_inputs(M, N, K, seed=42, op="ag")
+    rs = Case(A, W)
+    ag = G.Plan(M, N, K, op=G.OP_AG)
+    ag_ws = ag.new_workspace()
+    ag_A, ag_W = to_dev(A_ag), to_dev(W_ag)
+    ag_out = torch.empty(*ag.out_shape, dtype=torch.bfloat16, device="cuda")
+    rs_ref = rs.run(G.UNFUSED)
+    ag.run(ag_A, ag_W, ag_out, ag_ws, G.UNFUSED)
+    torch.cuda.synchronize()
+    ag_ref = ag_out.clone()
+    rs_outs = [torch.empty_like(rs.out) for _ in range(3)]
+    ag_outs = [torch.empty_like(ag_out) for _ in range(3)]
+    for i in range(3):
+        rs.plan.run(rs.A, rs.W, rs_outs[i], rs.ws, G.FUSED)
+        ag.run(ag_A, ag_W, ag_outs[i], ag_ws, G.FUSED)
+    torch.cuda.synchronize()
+    assert rs.plan.status() == G.GEMM_RS_OK and ag.status() == G.GEMM_RS_OK
+    for i in range(3):
+        assert torch.equal(rs_outs[i].view(torch.int16), rs_ref.view(torch.int16)), i
+        assert torch.equal(ag_outs[i].view(torch.int16), ag_ref.view(torch.int16)), i
+
+
 def test_empty_and_zero_k():
     p = G.Plan(0, 256, 512)
     ws = p.new_workspace()
