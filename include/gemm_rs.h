@@ -228,7 +228,11 @@ int gemm_rs_create(const gemm_rs_desc* d, gemm_rs_t* plan, size_t* workspace_byt
  * creates on its first CHUNKED call; that stream joins `stream` again before
  * the call returns (work after it on `stream` sees the whole output).  Modes
  * that do not read A/W (RS_ONLY) or write out (GEMM_ONLY) accept NULL for
- * them.
+ * them.  The GEMM kernels are launched with programmatic dependent launch:
+ * their CTAs may start setting up shared memory and TMEM while the previous
+ * kernel on `stream` finishes, but touch no global memory before that kernel
+ * has completed, so stream order holds for every buffer; a kernel queued
+ * after them that allows the same overlap may likewise start early and wait.
  */
 int gemm_rs_run(gemm_rs_t plan, int mode, const void* A, const void* W,
                 void* out, void* workspace, void* stream);
