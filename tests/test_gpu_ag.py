@@ -167,3 +167,6 @@ def test_workload_sampled(name):
     partial_ulp_check(fv, ref, absAW, w.K)
     unf = c.run(G.UNFUSED, poison=True)
     assert torch.equal(fused.view(torch.int16), unf.view(torch.int16))
+    if name == "llama3_70b_qkv_m2048":  # the same run with the shards moved by the copy engines
+        ce = AGCase(A, W, copy_engines=4)
+        assert torch.equal(ce.run(G.FUSED, poison=True).view(torch.int16), unf.view(torch.int16))
