@@ -1030,14 +1030,23 @@ __global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxRe
       const int nchunks = tc.half >= 0 ? kBN / 128 : kBN / 64;  // 64-column chunks of the tile
       const int col0 = tc.nt * kBN + (tc.half >= 0 ? tc.half * (kBN / 2) : 0);
 #pragma unroll 1
-      for (int c = 0; c < nchunks; ++c) {
-        uint32_t v0[32], v1[32];
-        const uint32_t taddr =
-            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + c * 64);
+      // chunk c + 1's TMEM loads are in flight while chunk c is packed,
+      // written to shared memory and stored
+      uint32_t v0[32], v1[32];
+      {
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
         tmem_ld_32x32b_x32(taddr, v0);
         tmem_ld_32x32b_x32(taddr + 32, v1);
+      }
+      for (int c = 0; c < nchunks; ++c) {
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
+        uint32_t w[32];  // the chunk's 64 columns of the lane's row as bf16 pairs
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          w[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+          w[16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+        }
         if (c == nchunks - 1) {
           // accumulator fully read: hand it back to the (leader's) MMA warp
           tc_fence_before();
@@ -1048,6 +1057,11 @@ __global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxRe
             else
               mbar_arrive_remote(mapa_shared(bar_acc_empty + 8 * acc, mma_leader_rank));
           }
+        } else {
+          const uint32_t taddr =
+              tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + (c + 1) * 64);
+          tmem_ld_32x32b_x32(taddr, v0);
+          tmem_ld_32x32b_x32(taddr + 32, v1);
         }
         const int col = col0 + c * 64;
         if (row0 < p.M && col < p.N) {  // warp-uniform; the store clips ragged edges
@@ -1055,14 +1069,9 @@ __global__ void __launch_bounds__(32 * cta_warps(kKind == kKindGemm ? 0 : kMaxRe
           if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
           __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {  // granule j = columns [8j, 8j + 8) of the lane's row
-            const uint32_t* v = (j < 4) ? (v0 + 8 * j) : (v1 + 8 * (j - 4));
-            st_shared_v4(buf + (uint32_t)((j ^ (lane & 7)) << 4),
-                         pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                         pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                         pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                         pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
-          }
+          for (int j = 0; j < 8; ++j)  // granule j = columns [8j, 8j + 8) of the lane's row
+            st_shared_v4(buf + (uint32_t)((j ^ (lane & 7)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                         w[4 * j + 3]);
           fence_proxy_async_shared();  // the writes, before the async proxy reads them
           __syncwarp();
           if (lane == 0) {
